@@ -1,0 +1,440 @@
+"""Benchmark: MoE top-k dispatch + combine on one GB300 (or N replicas).
+
+One step is the whole hot path on one batch of synthetic input, as the axolotl
+``integrations.expert_parallel.torch_dispatch`` page lays it out for the
+collective-free local path:
+
+    compute_send_counts -> one device->host copy of the counts ->
+    build_send_layout(num_send from the host) -> dispatch (row scatter) ->
+    combine (per-token sum of the expert outputs)
+
+on the large skewed workload (T=16384, H=7168 bf16, E=256, K=8, P=8 logical
+ranks, Zipf(1.2) routing).  Inputs are resident in HBM when a step starts; L2
+is flushed (512 MiB write) between steps, outside the timed events.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(plain C, one core) on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------ host helpers --
+def algorithmic_bytes(T: int, H: int, N: int, K: int, P: int) -> dict:
+    """Bytes the method must move (each source row read once, each
+    destination row written once), per kernel of one step."""
+    row = H * 2
+    return {
+        "counts": T * K * 8 + T * K * 4 + T * P,                       # idx in; dest, is_in_rank out
+        "layout": T * K * 8 + T * K * 4 + T * K * 4 + 2 * T * P + T * P * 4 + N * (8 + K * 12),
+        "dispatch": T * row + N * row + T * P * 4,
+        "combine": N * row + T * row + T * P * 4,
+    }
+
+
+def aggregate(local_seconds: float, local_units: float, world: int, dist=None) -> tuple:
+    """Whole-job throughput of N replicas: units summed over ranks, time is the
+    slowest rank's.  Returns (units_per_second, max_seconds)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([local_seconds], dtype=torch.float64)
+        u = torch.tensor([local_units], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            t, u = t.cuda(), u.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        local_seconds, local_units = float(t.item()), float(u.item())
+    return local_units / local_seconds, local_seconds
+
+
+def measured_peak() -> tuple:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "of measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_send_counts_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU arm --
+class SendPath:
+    """All device buffers of the send-layout path, allocated once."""
+
+    def __init__(self, ep, torch, w, x, idx, wts, dev):
+        self.ep, self.torch, self.w = ep, torch, w
+        T, K, P, El, H = w.T, w.K, w.P, w.E_local, w.H
+        self.x, self.idx, self.wts = x, idx, wts
+        i32, u8 = torch.int32, torch.uint8
+        self.dest = torch.empty((T, K), dtype=i32, device=dev)
+        self.is_in_rank = torch.empty((T, P), dtype=u8, device=dev)
+        self.send_counts = torch.empty((1, P), dtype=i32, device=dev)
+        self.rank_offsets = torch.empty((1, P + 1), dtype=i32, device=dev)
+        self.counts_h = torch.empty((1, P), dtype=i32, pin_memory=True)
+        self.ws = ep.workspace(T, K, P, El, 1, dev)
+        self.err = ep.error_word(dev)
+        self.token_pos = torch.empty((T, P), dtype=i32, device=dev)
+        self.N = None
+
+    def alloc_rows(self, N):
+        torch, w, dev = self.torch, self.w, self.x.device
+        self.N = N
+        self.send_token_idx = torch.empty(N, dtype=torch.int32, device=dev)
+        self.send_rank = torch.empty(N, dtype=torch.int32, device=dev)
+        self.send_idx = torch.empty((N, w.K), dtype=torch.int64, device=dev)
+        self.send_w = torch.empty((N, w.K), dtype=torch.float32, device=dev)
+        self.recv_x = torch.empty((N, w.H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+
+    def step(self, y, stream, ev=None):
+        """One pass of the hot path; ev = list of 5 events (or None)."""
+        ep, w = self.ep, self.w
+        T, K, P, El, H = w.T, w.K, w.P, w.E_local, w.H
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rec(0)
+        ep.ep_compute_send_counts(self.idx, T, K, P, El, None, 1, self.dest, self.is_in_rank, self.send_counts,
+                                  self.rank_offsets, None, self.ws, self.err, stream)
+        rec(1)
+        self.counts_h.copy_(self.send_counts, non_blocking=True)
+        stream.synchronize()
+        num_send = int(self.counts_h.sum())
+        if num_send != self.N:
+            raise RuntimeError(f"routed rows changed: {num_send} != {self.N}")
+        rec(2)
+        ep.ep_build_send_layout(self.idx, self.wts, self.dest, self.is_in_rank, T, K, P, El, num_send,
+                                self.send_token_idx, self.send_rank, self.send_idx, self.send_w,
+                                self.token_pos, self.ws, self.err, stream)
+        rec(3)
+        ep.ep_dispatch(self.x, T, H, self.token_pos, P, num_send, self.recv_x, None, 0, self.err, stream)
+        rec(4)
+        ep.ep_combine(y, T, H, self.token_pos, P, num_send, self.out, 0, self.err, stream)
+        rec(5)
+
+
+LAUNCHES_PER_STEP = 6   # counts: 2, layout: 2, dispatch: 1, combine: 1
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import combine_send_counts_gb300 as ep
+    from combine_send_counts_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    ep.load()
+
+    w = wl.WORKLOADS[args.workload]
+    x_h, idx_h, w_h = wl.make(w)
+    x, idx, wts = x_h.to(dev), idx_h.to(dev), w_h.to(dev)
+    sp = SendPath(ep, torch, w, x, idx, wts, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # size the rows from one count pass, then draw the expert outputs
+    ep.ep_compute_send_counts(idx, w.T, w.K, w.P, w.E_local, None, 1, sp.dest, sp.is_in_rank, sp.send_counts,
+                              sp.rank_offsets, None, sp.ws, sp.err, stream)
+    N = int(sp.send_counts.sum().item())
+    sp.alloc_rows(N)
+    y_h = wl.expert_outputs(w, N)
+    y = y_h.to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        sp.step(y, stream)
+    torch.cuda.synchronize()
+    if int(sp.err.item()) != 0:
+        raise ep.EPError(int(sp.err.item()), "warmup")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            sp.step(y, stream, evs[k])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if int(sp.err.item()) != 0:
+        raise ep.EPError(int(sp.err.item()), "timed steps")
+
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+    parts = {"counts": [e[0].elapsed_time(e[1]) for e in evs],
+             "counts_d2h_sync": [e[1].elapsed_time(e[2]) for e in evs],
+             "layout": [e[2].elapsed_time(e[3]) for e in evs],
+             "dispatch": [e[3].elapsed_time(e[4]) for e in evs],
+             "combine": [e[4].elapsed_time(e[5]) for e in evs]}
+    total_s = sum(step_ms) / 1e3
+    tok_s, max_s = aggregate(total_s, float(w.T * args.steps), world, dist if world > 1 else None)
+
+    peak, peak_src = measured_peak()
+    ab = algorithmic_bytes(w.T, w.H, N, w.K, w.P)
+    kern = {}
+    for name in ("counts", "layout", "dispatch", "combine"):
+        us = statistics.mean(parts[name]) * 1e3
+        kern[name] = {"us": round(us, 2), "algorithmic_bytes": ab[name],
+                      "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1)}
+    kern["counts_d2h_sync"] = {"us": round(statistics.mean(parts["counts_d2h_sync"]) * 1e3, 2)}
+    dom = max(("dispatch", "combine"), key=lambda k: kern[k]["us"])
+    step_bytes = sum(ab.values())
+    mean_step_ms = statistics.mean(step_ms)
+    achieved_step = step_bytes / (mean_step_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(tok_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: T={w.T} H={w.H} E={w.E} K={w.K} P={w.P} E_local={w.E_local} "
+                               f"routing={w.routing}({w.zipf_s}) weights={w.weights}",
+                   "N_rows": N, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (512 MiB write, outside the timed events); "
+                         "working set 1.8 GB > L2",
+                   "path": "counts -> D2H counts + host sync -> layout -> dispatch -> combine",
+                   "seed": w.seed},
+        "hbm_gbs": round(achieved_step, 1),
+        "hbm_frac_of_peak": round(achieved_step / peak, 4),
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(kern[dom]["gbs"] / peak, 4),
+                     "traffic": committed_traffic(dom),
+                     "algorithmic_bytes_per_launch": ab[dom]},
+        "kernels": kern,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, stream, world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, x_h, idx_h, w_h, y_h, args.cpu_steps, full=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, stream, world, dist):
+    """Same step through the C ABI from pinned HOST buffers: H2D of the inputs
+    and the expert outputs, the path, D2H of the combined result, all inside
+    the timed events."""
+    xp, ip, wp, yp = (t.pin_memory() for t in (x_h, idx_h, w_h, y_h))
+    outp = torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True)
+    y_d = torch.empty_like(yp, device=sp.x.device)
+    h2d = sum(t.numel() * t.element_size() for t in (xp, ip, wp, yp))
+    d2h = outp.numel() * outp.element_size() + w.P * 4
+    times = []
+    for k in range(args.e2e_warmup + args.e2e_steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sp.x.copy_(xp, non_blocking=True)
+        sp.idx.copy_(ip, non_blocking=True)
+        sp.wts.copy_(wp, non_blocking=True)
+        y_d.copy_(yp, non_blocking=True)
+        sp.step(y_d, stream)
+        outp.copy_(sp.out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if k >= args.e2e_warmup:
+            times.append(a.elapsed_time(b) / 1e3)
+    tok_s, _ = aggregate(sum(times), float(w.T * len(times)), world, dist if world > 1 else None)
+    return {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": len(times)}
+
+
+# ------------------------------------------------------------------ CPU arm --
+def oracle_step(oracle, w, x, idx, wts, y):
+    o = oracle.send_path(x, idx, wts, None, w.P, w.E_local)
+    return oracle.combine(y[:o["layout"]["n"]], o["layout"]["token_pos"])
+
+
+def cpu_baseline(w, x, idx, wts, y, steps, full=True, T_sample=None):
+    import oracle
+    if T_sample is not None and T_sample < w.T:
+        x, idx, wts = x[:T_sample], idx[:T_sample], wts[:T_sample]
+    T = x.shape[0]
+    oracle_step(oracle, w, x[:64], idx[:64], wts[:64], y)   # load / build
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(oracle, w, x, idx, wts, y)
+    dt = time.perf_counter() - t0
+    return {"value": round(T * steps / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} step(s) of the send path (counts, layout, dispatch, combine) on the first "
+                      f"{T} of {w.T} tokens of the {w.name} workload, single-threaded C oracle"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is the send path on a bounded
+    sample (the first T_sample tokens) of the same workload, on one host core."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from combine_send_counts_gb300 import workloads as wl
+    import oracle
+    w = wl.WORKLOADS[args.workload]
+    x, idx, wts = wl.make(w)
+    Ts = min(args.reference_tokens, w.T)
+    x, idx, wts = x[:Ts], idx[:Ts], wts[:Ts]
+    c = oracle.compute_send_counts(idx, w.P, w.E_local, with_tokens_per_expert=False)
+    y = wl.expert_outputs(w, int(c["send_counts"].sum()))
+    for _ in range(max(args.warmup, 0)):
+        oracle_step(oracle, w, x, idx, wts, y)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(oracle, w, x, idx, wts, y)
+        times.append(time.perf_counter() - t0)
+    tok_s = Ts * len(times) / sum(times)
+    sample = (f"first {Ts} of {w.T} tokens of the {w.name} workload per step; send path (counts, layout, "
+              f"dispatch, combine) in the single-threaded C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: T={w.T} H={w.H} E={w.E} K={w.K} P={w.P} E_local={w.E_local} "
+                               f"routing={w.routing}({w.zipf_s}) weights={w.weights}", "T_sample": Ts},
+        "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="large")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-warmup", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-steps", type=int, default=4)
+    ap.add_argument("--reference-tokens", type=int, default=4096)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,330 @@
+"""GB300 (sm_103a) MoE top-k token dispatch / combine.
+
+Thin ctypes binding over ``libep_gb300.so`` (C ABI in ``include/ep.h``).  The
+``ep_*`` functions here have the same names and argument order as the C
+entry points and only marshal arguments: torch tensors become device pointers,
+the current CUDA stream is passed through, and a non-OK status raises
+:class:`EPError`.  Every step runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback, and using the binding without the built library on a
+CUDA device raises.
+
+The lower-case helpers at the end (``compute_send_counts``,
+``build_send_layout``, ``dispatch``, ``combine``, ``batched_prepare``,
+``batched_combine``, ``chunk_bounds``) allocate outputs with torch and call
+the ``ep_*`` entry points; they follow the call shapes of the axolotl
+``integrations.expert_parallel.torch_dispatch`` page and the vLLM
+``BatchedPrepareAndFinalize`` page.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import _build
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_INVALID_EXPERT = 2
+EP_ERR_COUNT_MISMATCH = 4
+EP_ERR_CAPACITY = 8
+EP_ERR_UNSUPPORTED = 16
+EP_ERR_CUDA = 32
+EP_ERR_TIMEOUT = 64
+
+_ERR_NAMES = {
+    EP_ERR_INVALID_ARG: "EP_ERR_INVALID_ARG", EP_ERR_INVALID_EXPERT: "EP_ERR_INVALID_EXPERT",
+    EP_ERR_COUNT_MISMATCH: "EP_ERR_COUNT_MISMATCH", EP_ERR_CAPACITY: "EP_ERR_CAPACITY",
+    EP_ERR_UNSUPPORTED: "EP_ERR_UNSUPPORTED", EP_ERR_CUDA: "EP_ERR_CUDA",
+    EP_ERR_TIMEOUT: "EP_ERR_TIMEOUT",
+}
+
+
+class EPError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        names = [n for b, n in _ERR_NAMES.items() if status & b] or [str(status)]
+        super().__init__(f"{where}: {'|'.join(names)}" if where else "|".join(names))
+        self.status = status
+
+
+_lib = None
+_VP, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+
+_SIGNATURES = {
+    "ep_status_str": (ctypes.c_char_p, [_I32]),
+    "ep_workspace_size": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
+    "ep_chunk_bounds": (_I32, [_I64, _I32, _VP]),
+    "ep_compute_send_counts": (_I32, [_VP, _I64, _I32, _I32, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
+                                      _VP, _SZ, _VP, _VP]),
+    "ep_build_send_layout": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I64, _VP, _VP, _VP, _VP,
+                                    _VP, _VP, _SZ, _VP, _VP]),
+    "ep_dispatch": (_I32, [_VP, _I64, _I32, _VP, _I32, _I64, _VP, _VP, _I32, _VP, _VP]),
+    "ep_combine": (_I32, [_VP, _I64, _I32, _VP, _I32, _I64, _VP, _I32, _VP, _VP]),
+    "ep_batched_prepare": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32,
+                                  _VP, _SZ, _VP, _VP]),
+    "ep_batched_combine": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "ep_local_expert_fp8": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libep_gb300.so (building it first if asked and needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libep_gb300.so is not built ({path}); run combine_send_counts_gb300._build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, where: str):
+    if rc != EP_OK:
+        raise EPError(rc, where)
+
+
+# ------------------------------------------------------------- C ABI names --
+def ep_status_str(status: int) -> str:
+    return load().ep_status_str(int(status)).decode()
+
+
+def ep_workspace_size(T: int, K: int, P: int, E_local: int, chunks: int = 1) -> int:
+    return int(load().ep_workspace_size(int(T), int(K), int(P), int(E_local), int(chunks)))
+
+
+def ep_chunk_bounds(T: int, chunks: int) -> list:
+    buf = (ctypes.c_int64 * (chunks + 1))()
+    _check(load().ep_chunk_bounds(int(T), int(chunks), buf), "ep_chunk_bounds")
+    return list(buf)
+
+
+def ep_compute_send_counts(topk_idx, T, K, P, E_local, h_chunk_bounds, chunks, dest, is_in_rank,
+                           send_counts, rank_offsets, tokens_per_expert, ws, err, stream=None):
+    hb = None
+    if h_chunk_bounds is not None:
+        hb = (ctypes.c_int64 * len(h_chunk_bounds))(*[int(v) for v in h_chunk_bounds])
+    rc = load().ep_compute_send_counts(_p(topk_idx), int(T), int(K), int(P), int(E_local), hb, int(chunks),
+                                       _p(dest), _p(is_in_rank), _p(send_counts), _p(rank_offsets),
+                                       _p(tokens_per_expert), _p(ws), ws.numel() * ws.element_size(),
+                                       _p(err), _stream(stream))
+    _check(rc, "ep_compute_send_counts")
+
+
+def ep_build_send_layout(topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_send,
+                         send_token_idx, send_rank, send_idx, send_w, token_pos, ws, err, stream=None):
+    rc = load().ep_build_send_layout(_p(topk_idx), _p(topk_weights), _p(dest), _p(is_in_rank), int(T), int(K),
+                                     int(P), int(E_local), int(num_send), _p(send_token_idx), _p(send_rank),
+                                     _p(send_idx), _p(send_w), _p(token_pos), _p(ws),
+                                     ws.numel() * ws.element_size(), _p(err), _stream(stream))
+    _check(rc, "ep_build_send_layout")
+
+
+def ep_dispatch(x, T, H, token_pos, P, num_send, recv_x, recv_scale, fp8, err, stream=None):
+    rc = load().ep_dispatch(_p(x), int(T), int(H), _p(token_pos), int(P), int(num_send), _p(recv_x),
+                            _p(recv_scale), int(fp8), _p(err), _stream(stream))
+    _check(rc, "ep_dispatch")
+
+
+def ep_combine(y, T, H, token_pos, P, num_send, out, out_dtype, err, stream=None):
+    rc = load().ep_combine(_p(y), int(T), int(H), _p(token_pos), int(P), int(num_send), _p(out),
+                           int(out_dtype), _p(err), _stream(stream))
+    _check(rc, "ep_combine")
+
+
+def ep_batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b_x, tokens_per_expert,
+                       slot, zero_pad, ws, err, stream=None):
+    rc = load().ep_batched_prepare(_p(x), _p(topk_idx), int(T), int(K), int(H), int(E), int(E_local),
+                                   int(rank), int(max_num_tokens), _p(b_x), _p(tokens_per_expert), _p(slot),
+                                   int(zero_pad), _p(ws), ws.numel() * ws.element_size(), _p(err),
+                                   _stream(stream))
+    _check(rc, "ep_batched_prepare")
+
+
+def ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, E_local, rank, max_num_tokens, out, err,
+                       stream=None):
+    rc = load().ep_batched_combine(_p(y), _p(topk_idx), _p(topk_weights), _p(slot), int(T), int(K), int(H),
+                                   int(E_local), int(rank), int(max_num_tokens), _p(out), _p(err),
+                                   _stream(stream))
+    _check(rc, "ep_batched_combine")
+
+
+def ep_local_expert_fp8(recv_q, recv_scale, send_idx, send_w, N, K, H, out, err, stream=None):
+    rc = load().ep_local_expert_fp8(_p(recv_q), _p(recv_scale), _p(send_idx), _p(send_w), int(N), int(K),
+                                    int(H), _p(out), _p(err), _stream(stream))
+    _check(rc, "ep_local_expert_fp8")
+
+
+# ------------------------------------------------------------------ helpers --
+def workspace(T: int, K: int, P: int, E_local: int, chunks: int = 1, device=None) -> torch.Tensor:
+    """A device workspace of ep_workspace_size bytes (torch allocations are 256-B aligned)."""
+    n = max(ep_workspace_size(T, K, P, E_local, chunks), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def error_word(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def raise_device_error(err: torch.Tensor, where: str = "device"):
+    """Synchronise and raise EPError if the device error word is non-zero."""
+    v = int(err.item())
+    if v:
+        raise EPError(v, where)
+
+
+def chunk_bounds(num_tokens: int, chunks: int) -> list:
+    return ep_chunk_bounds(num_tokens, chunks)
+
+
+def compute_send_counts(topk_idx: torch.Tensor, num_ranks: int, num_local_experts: int,
+                        chunk_bounds: Optional[Sequence[int]] = None, ws=None, err=None, stream=None,
+                        with_tokens_per_expert: bool = True):
+    """-> dict(dest, is_in_rank, send_counts [C,P], rank_offsets [C,P+1], tokens_per_expert)."""
+    T, K = topk_idx.shape
+    P, El = num_ranks, num_local_experts
+    C = len(chunk_bounds) - 1 if chunk_bounds is not None else 1
+    dev = topk_idx.device
+    out = dict(
+        dest=torch.empty((T, K), dtype=torch.int32, device=dev),
+        is_in_rank=torch.empty((T, P), dtype=torch.uint8, device=dev),
+        send_counts=torch.empty((C, P), dtype=torch.int32, device=dev),
+        rank_offsets=torch.empty((C, P + 1), dtype=torch.int32, device=dev),
+        tokens_per_expert=torch.empty(P * El, dtype=torch.int32, device=dev) if with_tokens_per_expert else None,
+    )
+    ws = ws if ws is not None else workspace(T, K, P, El, C, dev)
+    err = err if err is not None else error_word(dev)
+    ep_compute_send_counts(topk_idx, T, K, P, El, chunk_bounds if C > 1 else None, C, out["dest"],
+                           out["is_in_rank"], out["send_counts"], out["rank_offsets"], out["tokens_per_expert"],
+                           ws, err, stream)
+    out["err"] = err
+    return out
+
+
+def build_send_layout(topk_idx, topk_weights, dest, is_in_rank, num_send: int, num_local_experts: int,
+                      ws=None, err=None, stream=None):
+    """-> dict(send_token_idx [N], send_rank [N], send_idx [N,K], send_w [N,K], token_pos [T,P])."""
+    T, K = topk_idx.shape
+    P = is_in_rank.shape[1]
+    dev = topk_idx.device
+    N = int(num_send)
+    out = dict(
+        send_token_idx=torch.empty(N, dtype=torch.int32, device=dev),
+        send_rank=torch.empty(N, dtype=torch.int32, device=dev),
+        send_idx=torch.empty((N, K), dtype=torch.int64, device=dev),
+        send_w=torch.empty((N, K), dtype=torch.float32, device=dev),
+        token_pos=torch.empty((T, P), dtype=torch.int32, device=dev),
+    )
+    ws = ws if ws is not None else workspace(T, K, P, num_local_experts, 1, dev)
+    err = err if err is not None else error_word(dev)
+    ep_build_send_layout(topk_idx, topk_weights, dest, is_in_rank, T, K, P, num_local_experts, N,
+                         out["send_token_idx"], out["send_rank"], out["send_idx"], out["send_w"],
+                         out["token_pos"], ws, err, stream)
+    out["err"] = err
+    return out
+
+
+def dispatch_rows(x: torch.Tensor, token_pos: torch.Tensor, num_send: int, fp8: bool = False, err=None,
+                  stream=None):
+    """recv_x [N,H] bf16, or (recv_q [N,H] e4m3 as uint8, recv_scale [N,H/128] fp32) when fp8."""
+    T, H = x.shape
+    P = token_pos.shape[1]
+    err = err if err is not None else error_word(x.device)
+    if fp8:
+        q = torch.empty((num_send, H), dtype=torch.uint8, device=x.device)
+        s = torch.empty((num_send, H // 128), dtype=torch.float32, device=x.device)
+        ep_dispatch(x, T, H, token_pos, P, num_send, q, s, 1, err, stream)
+        return q, s
+    recv = torch.empty((num_send, H), dtype=x.dtype, device=x.device)
+    ep_dispatch(x, T, H, token_pos, P, num_send, recv, None, 0, err, stream)
+    return recv
+
+
+def combine_rows(y: torch.Tensor, token_pos: torch.Tensor, out_dtype=torch.bfloat16, err=None, stream=None):
+    T, P = token_pos.shape
+    N, H = y.shape
+    out = torch.empty((T, H), dtype=out_dtype, device=y.device)
+    err = err if err is not None else error_word(y.device)
+    ep_combine(y, T, H, token_pos, P, N, out, 1 if out_dtype == torch.float32 else 0, err, stream)
+    return out
+
+
+def dispatch(x, topk_idx, topk_weights, *, num_local_experts: int, num_ranks: int, fp8: bool = False):
+    """The collective-free local path of the axolotl dispatch: counts, one
+    device-to-host copy of the counts, layout, row scatter.
+    Returns (recv_x, recv_idx, recv_w, handle)."""
+    c = compute_send_counts(topk_idx, num_ranks, num_local_experts, with_tokens_per_expert=False)
+    num_send = int(c["send_counts"].sum().item())
+    lay = build_send_layout(topk_idx, topk_weights, c["dest"], c["is_in_rank"], num_send, num_local_experts)
+    recv = dispatch_rows(x, lay["token_pos"], num_send, fp8=fp8)
+    handle = dict(num_tokens=x.shape[0], token_pos=lay["token_pos"], send_counts=c["send_counts"],
+                  send_token_idx=lay["send_token_idx"], err=c["err"])
+    return recv, lay["send_idx"], lay["send_w"], handle
+
+
+def combine(local_out: torch.Tensor, handle: dict, dtype=None):
+    return combine_rows(local_out, handle["token_pos"], out_dtype=dtype or torch.bfloat16)
+
+
+def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int,
+                    zero_pad: bool = False, err=None, stream=None):
+    """-> dict(b_x [E_local,M,H], tokens_per_expert [E_local], slot [T,K])."""
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    El = num_local_experts
+    dev = x.device
+    b_x = torch.empty((El, max_num_tokens, H), dtype=x.dtype, device=dev)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws = workspace(T, K, num_experts // El, El, 1, dev)
+    err = err if err is not None else error_word(dev)
+    ep_batched_prepare(x, topk_idx, T, K, H, num_experts, El, rank, max_num_tokens, b_x, tpe, slot,
+                       int(zero_pad), ws, err, stream)
+    return dict(b_x=b_x, tokens_per_expert=tpe, slot=slot, err=err)
+
+
+def batched_combine(y, topk_idx, topk_weights, slot, rank: int, err=None, stream=None):
+    El, M, H = y.shape
+    T, K = topk_idx.shape
+    out = torch.empty((T, H), dtype=y.dtype, device=y.device)
+    err = err if err is not None else error_word(y.device)
+    ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, El, rank, M, out, err, stream)
+    return out
+
+
+def local_expert_fp8(recv_q, recv_scale, send_idx, send_w, err=None, stream=None):
+    N, H = recv_q.shape
+    K = send_idx.shape[1]
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=recv_q.device)
+    err = err if err is not None else error_word(recv_q.device)
+    ep_local_expert_fp8(recv_q, recv_scale, send_idx, send_w, N, K, H, out, err, stream)
+    return out

@@ -1,0 +1,45 @@
+// Host-side helpers shared by the translation units of libep_gb300.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ep.h"
+
+namespace ep {
+
+constexpr int kRouteThreads = 256;   // = tokens per routing block
+constexpr size_t kWsAlign = 256;
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Launch status of the most recent kernel launch on this thread.
+inline int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+// Upper bound on routing blocks for T tokens split into `chunks` ranges.
+inline int64_t route_blocks_max(int64_t T, int chunks)
+{
+    return ceil_div(T, kRouteThreads) + (chunks > 1 ? chunks : 1);
+}
+
+// Per-chunk block decomposition for the routing kernels: block b belongs to
+// the chunk c with first_block[c] <= b < first_block[c+1] and covers tokens
+// start[c] + (b - first_block[c]) * 256 ... (clipped to start[c+1]).
+struct ChunkTable {
+    int n;
+    int first_block[EP_MAX_CHUNKS + 1];
+    int64_t start[EP_MAX_CHUNKS + 1];
+};
+
+// Launchers implemented in ep_route.cu and used by the batched entry points.
+int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
+                         int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
+                         int32_t *part, int32_t *err, cudaStream_t stream);
+
+}  // namespace ep

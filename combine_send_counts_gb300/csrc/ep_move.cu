@@ -1,0 +1,582 @@
+// Row movement kernels of libep_gb300.
+//
+//   scatter  -- dispatch (axolotl integrations.expert_parallel.torch_dispatch,
+//               dispatch; NeMo uccl_ep.buffer, Buffer.dispatch) and the
+//               expert-batched prepare (vLLM BatchedPrepareAndFinalize.prepare):
+//               every source row is read from HBM once and written to each of
+//               its destination rows.
+//   gather   -- combine (axolotl combine; Buffer.combine, addition without
+//               weights) and the batched combine (BatchedPrepareAndFinalize
+//               .finalize; Buffer.low_latency_combine, reduce with weights):
+//               every output row reads its source rows in a fixed order,
+//               accumulates in fp32 and is written once.
+//
+// Both are HBM-bound copies.  A group of G threads (a multiple of 32) owns one
+// token; each thread moves U 16-byte vectors of the row, so a row is covered
+// in one pass for H up to 8*G*U.  The destination (or source) row list of the
+// block's tokens is resolved once into shared memory.
+#include <algorithm>
+#include <climits>
+
+#include <cuda_fp16.h>
+
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+
+constexpr int kMoveThreads = 256;
+constexpr int kMaxList = 64;               // >= max(P, K)
+constexpr int kMaxTokensPerBlock = kMoveThreads / 32;
+
+// ------------------------------------------------------- row list sources --
+// Send layout: the rows of token t are token_pos[t, p] (p ascending), -1 = none.
+struct SendRows {
+    const int32_t *token_pos;
+    int P;
+    __device__ __forceinline__ int len() const { return P; }
+    __device__ __forceinline__ int32_t row(int64_t t, int j) const { return token_pos[t * P + j]; }
+    __device__ __forceinline__ float weight(int64_t, int) const { return 1.0f; }
+};
+
+// Expert-batched layout: slot k of token t names local expert e_l and slot s:
+// row e_l * M + s.  `dedup` drops a slot naming the same expert as an earlier
+// slot of the token (the scatter writes each (expert, token) row once; the
+// weighted combine keeps every slot's term).
+struct BatchedRows {
+    const int64_t *idx;
+    const int32_t *slot;
+    const float *w;
+    int K;
+    int64_t e0;
+    int E_local;
+    int M;
+    bool dedup;
+    __device__ __forceinline__ int len() const { return K; }
+    __device__ __forceinline__ int32_t row(int64_t t, int j) const
+    {
+        const int32_t s = slot[t * K + j];
+        const int64_t id = idx[t * K + j];
+        const int64_t el = id - e0;
+        if (s < 0 || el < 0 || el >= E_local)
+            return -1;
+        if (s >= M)                     // not a slot of this layout: reported by the caller
+            return INT32_MAX;
+        if (dedup)
+            for (int i = 0; i < j; ++i)
+                if (idx[t * K + i] == id)
+                    return -1;
+        return (int32_t)(el * M + s);
+    }
+    __device__ __forceinline__ float weight(int64_t t, int j) const { return w ? w[t * K + j] : 1.0f; }
+};
+
+struct Geometry {
+    int nvec;   // 16-byte vectors per row (H / 8 for bf16)
+    int G;      // threads per token
+    int tpb;    // tokens per block
+};
+
+// Resolve the row lists of this block's tokens into shared memory; rows that
+// fall outside [0, n_rows) are reported and dropped.
+template <class Rows>
+__device__ __forceinline__ void load_lists(const Rows &rows, int64_t T, int64_t t0, int tpb,
+                                           int64_t n_rows, int err_bits, int32_t *s_rows,
+                                           float *s_w, int32_t *err)
+{
+    const int D = rows.len();
+    int bad = 0;
+    for (int i = threadIdx.x; i < tpb * D; i += blockDim.x) {
+        const int s = i / D, j = i % D;
+        const int64_t t = t0 + s;
+        int32_t r = -1;
+        float wv = 0.0f;
+        if (t < T) {
+            r = rows.row(t, j);
+            if (r >= n_rows) {
+                bad = err_bits;
+                r = -1;
+            }
+            if (r >= 0 && s_w != nullptr)
+                wv = rows.weight(t, j);
+        }
+        s_rows[s * kMaxList + j] = r;
+        if (s_w != nullptr)
+            s_w[s * kMaxList + j] = wv;
+    }
+    raise(err, bad);
+}
+
+// ---------------------------------------------------------- bf16 scatter --
+template <int U, class Rows>
+__global__ void __launch_bounds__(kMoveThreads)
+scatter_bf16_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows, int64_t n_rows,
+                    int err_bits, uint4 *__restrict__ out, int32_t *err)
+{
+    __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
+    const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
+    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
+    __syncthreads();
+    const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
+    const int64_t t = t0 + s;
+    if (s >= g.tpb || t >= T)
+        return;
+    const int D = rows.len();
+    const int32_t *list = s_rows + s * kMaxList;
+    const uint4 *src = x + t * g.nvec;
+    for (int base = 0; base < g.nvec; base += g.G * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + lt + u * g.G;
+            if (i < g.nvec)
+                v[u] = ld_stream(src + i);
+        }
+        for (int j = 0; j < D; ++j) {
+            const int32_t r = list[j];
+            if (r < 0)
+                continue;
+            uint4 *dst = out + (int64_t)r * g.nvec;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + lt + u * g.G;
+                if (i < g.nvec)
+                    st_stream(dst + i, v[u]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------- fp8 (1x128) scatter --
+// Quantises each source row once, in 128-element groups (16 vectors, held by
+// 16 consecutive lanes because G is a multiple of 32), and writes the e4m3
+// codes and the fp32 group scales to each destination row:
+//   a = max(max|x|, 1e-4), q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448.
+template <int U, class Rows>
+__global__ void __launch_bounds__(kMoveThreads)
+scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows, int64_t n_rows,
+                   int err_bits, uint2 *__restrict__ out_q, float *__restrict__ out_scale, int32_t *err)
+{
+    __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
+    const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
+    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
+    __syncthreads();
+    const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
+    const int64_t t = t0 + s;
+    if (s >= g.tpb || t >= T)
+        return;
+    const int D = rows.len();
+    const int groups = g.nvec / 16;
+    const int32_t *list = s_rows + s * kMaxList;
+    const uint4 *src = x + t * g.nvec;
+    for (int base = 0; base < g.nvec; base += g.G * U) {
+        uint2 q[U];
+        float scale[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + lt + u * g.G;
+            const bool ok = i < g.nvec;            // uniform over each half-warp
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (ok)
+                v = ld_stream(src + i);
+            float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                          bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+            const float a = fmaxf(amax, 1e-4f);
+            const float inv = __fdiv_rn(448.0f, a);
+            uint32_t packed[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 pr = make_float2(__fmul_rn(f[2 * e], inv), __fmul_rn(f[2 * e + 1], inv));
+                packed[e] = (uint32_t)__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
+            }
+            q[u] = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
+            scale[u] = __fdiv_rn(a, 448.0f);
+        }
+        for (int j = 0; j < D; ++j) {
+            const int32_t r = list[j];
+            if (r < 0)
+                continue;
+            uint2 *dq = out_q + (int64_t)r * g.nvec;
+            float *ds = out_scale + (int64_t)r * groups;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + lt + u * g.G;
+                if (i < g.nvec) {
+                    st_stream(dq + i, q[u]);
+                    if ((lt & 15) == 0)
+                        ds[i >> 4] = scale[u];
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------- gather-reduce --
+// out[t] = sum_j w_j * y[row_j] over the token's list in order, fp32, from
+// +0.0f: a plain add when unweighted (send-layout combine), a fused
+// multiply-add when weighted (batched combine).
+template <int U, class Rows, bool WEIGHTED, bool OUT_F32>
+__global__ void __launch_bounds__(kMoveThreads)
+gather_kernel(const uint4 *__restrict__ y, int64_t T, Geometry g, Rows rows, int64_t n_rows,
+              int err_bits, void *__restrict__ out, int32_t *err)
+{
+    __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
+    __shared__ float s_w[WEIGHTED ? kMaxTokensPerBlock * kMaxList : 1];
+    const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
+    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, WEIGHTED ? s_w : nullptr, err);
+    __syncthreads();
+    const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
+    const int64_t t = t0 + s;
+    if (s >= g.tpb || t >= T)
+        return;
+    const int D = rows.len();
+    const int32_t *list = s_rows + s * kMaxList;
+    for (int base = 0; base < g.nvec; base += g.G * U) {
+        float acc[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[u][e] = 0.0f;
+        for (int j = 0; j < D; ++j) {
+            const int32_t r = list[j];
+            if (r < 0)
+                continue;
+            const float wj = WEIGHTED ? s_w[s * kMaxList + j] : 1.0f;
+            const uint4 *src = y + (int64_t)r * g.nvec;
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + lt + u * g.G;
+                v[u] = i < g.nvec ? ld_stream(src + i) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                                    bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[u][e] = WEIGHTED ? __fmaf_rn(wj, f[e], acc[u][e]) : __fadd_rn(acc[u][e], f[e]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + lt + u * g.G;
+            if (i >= g.nvec)
+                continue;
+            if (OUT_F32) {
+                float4 *o = reinterpret_cast<float4 *>(out) + (t * g.nvec + i) * 2;
+                o[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+                o[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+            } else {
+                uint4 o;
+                o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                st_stream(reinterpret_cast<uint4 *>(out) + t * g.nvec + i, o);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- zero padding --
+// Zero rows [tokens_per_expert[e], M) of every local expert (16-byte stores).
+__global__ void zero_pad_kernel(uint4 *__restrict__ b_x, const int32_t *__restrict__ tokens_per_expert,
+                                int M, int nvec)
+{
+    const int e = blockIdx.y;
+    const int64_t first = (int64_t)tokens_per_expert[e] * nvec;
+    const int64_t total = (int64_t)M * nvec;
+    uint4 *base = b_x + (int64_t)e * total;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t i = first + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x)
+        st_stream(base + i, z);
+}
+
+// -------------------------------------------------- synthetic fp8 expert --
+// One block per row: d = e4m3(q) * scale, y_k = bf16(d * (1 + l_k/64)),
+// out = bf16(fma over k ascending of w_k * y_k from +0.0f).
+__global__ void __launch_bounds__(256)
+local_expert_fp8_kernel(const uint4 *__restrict__ q, const float *__restrict__ scale,
+                        const int64_t *__restrict__ send_idx, const float *__restrict__ send_w,
+                        int64_t N, int K, int H, uint4 *__restrict__ out)
+{
+    __shared__ float s_fac[EP_MAX_TOPK];
+    __shared__ float s_w[EP_MAX_TOPK];
+    __shared__ int s_n;
+    const int64_t n = blockIdx.x;
+    if (threadIdx.x == 0) {
+        int m = 0;
+        for (int k = 0; k < K; ++k) {
+            const int64_t l = send_idx[n * K + k];
+            if (l >= 0) {
+                s_fac[m] = __fadd_rn(1.0f, __fmul_rn((float)l, 0.015625f));
+                s_w[m] = send_w[n * K + k];
+                ++m;
+            }
+        }
+        s_n = m;
+    }
+    __syncthreads();
+    const int m = s_n;
+    const int chunks = H / 16;   // 16 codes per 16-byte vector
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        const uint4 v = q[n * chunks + c];
+        const float sc = scale[n * (H / 128) + c / 8];
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint32_t packed[8];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(words[wi] >> (16 * hh));
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+                const float2 d2 = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                const float d0 = __fmul_rn(d2.x, sc), d1 = __fmul_rn(d2.y, sc);
+                float a0 = 0.0f, a1 = 0.0f;
+                for (int k = 0; k < m; ++k) {
+                    const float y0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(d0, s_fac[k])));
+                    const float y1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(d1, s_fac[k])));
+                    a0 = __fmaf_rn(s_w[k], y0, a0);
+                    a1 = __fmaf_rn(s_w[k], y1, a1);
+                }
+                packed[wi * 2 + hh] = pack_bf16x2(a0, a1);
+            }
+        }
+        uint4 *o = out + (n * chunks + c) * 2;
+        o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+}
+
+// ------------------------------------------------------------ launch policy --
+static Geometry geometry_for(int nvec, int &U)
+{
+    U = nvec > 512 ? 8 : nvec > 256 ? 4 : nvec > 128 ? 2 : 1;
+    int G = (int)ceil_div(ceil_div(nvec, U), 32) * 32;
+    G = std::min(G, kMoveThreads);
+    Geometry g;
+    g.nvec = nvec;
+    g.G = G;
+    g.tpb = kMoveThreads / G;
+    return g;
+}
+
+template <class Rows>
+static int launch_scatter_bf16(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
+                               int err_bits, void *out, int32_t *err, cudaStream_t stream)
+{
+    int U;
+    const Geometry g = geometry_for(H / 8, U);
+    const int64_t blocks = ceil_div(T, g.tpb);
+    if (blocks == 0)
+        return EP_OK;
+    auto *xs = static_cast<const uint4 *>(x);
+    auto *o = static_cast<uint4 *>(out);
+    switch (U) {
+    case 8: scatter_bf16_kernel<8><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
+    case 4: scatter_bf16_kernel<4><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
+    case 2: scatter_bf16_kernel<2><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
+    default: scatter_bf16_kernel<1><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
+    }
+    return launch_status();
+}
+
+template <class Rows>
+static int launch_scatter_fp8(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
+                              int err_bits, void *out_q, float *out_scale, int32_t *err,
+                              cudaStream_t stream)
+{
+    int U;
+    const Geometry g = geometry_for(H / 8, U);
+    const int64_t blocks = ceil_div(T, g.tpb);
+    if (blocks == 0)
+        return EP_OK;
+    auto *xs = static_cast<const uint4 *>(x);
+    auto *q = static_cast<uint2 *>(out_q);
+    switch (U) {
+    case 8: scatter_fp8_kernel<8><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
+    case 4: scatter_fp8_kernel<4><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
+    case 2: scatter_fp8_kernel<2><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
+    default: scatter_fp8_kernel<1><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
+    }
+    return launch_status();
+}
+
+template <bool WEIGHTED, bool OUT_F32, class Rows>
+static int launch_gather(const void *y, int64_t T, int H, const Rows &rows, int64_t n_rows,
+                         int err_bits, void *out, int32_t *err, cudaStream_t stream)
+{
+    int U;
+    const Geometry g = geometry_for(H / 8, U);
+    const int64_t blocks = ceil_div(T, g.tpb);
+    if (blocks == 0)
+        return EP_OK;
+    auto *ys = static_cast<const uint4 *>(y);
+    switch (U) {
+    case 8: gather_kernel<8, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
+    case 4: gather_kernel<4, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
+    case 2: gather_kernel<2, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
+    default: gather_kernel<1, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
+    }
+    return launch_status();
+}
+
+static bool row_shape_ok(int64_t T, int H)
+{
+    return T >= 0 && H >= 8 && H % 8 == 0 && T < ((int64_t)1 << 31);
+}
+
+}  // namespace ep
+
+// ================================================================ C ABI ====
+using namespace ep;
+
+extern "C" const char *ep_status_str(int status)
+{
+    switch (status) {
+    case EP_OK: return "EP_OK";
+    case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+    case EP_ERR_INVALID_EXPERT: return "EP_ERR_INVALID_EXPERT";
+    case EP_ERR_COUNT_MISMATCH: return "EP_ERR_COUNT_MISMATCH";
+    case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
+    case EP_ERR_UNSUPPORTED: return "EP_ERR_UNSUPPORTED";
+    case EP_ERR_CUDA: return "EP_ERR_CUDA";
+    case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+    default: return "EP_ERR_(combination)";
+    }
+}
+
+extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P,
+                           int64_t num_send, void *recv_x, float *recv_scale, int fp8, int32_t *err,
+                           ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!row_shape_ok(T, H) || P < 1 || P > EP_MAX_RANKS || num_send < 0 || num_send >= ((int64_t)1 << 31))
+        return EP_ERR_INVALID_ARG;
+    if (fp8 != 0 && fp8 != 1)
+        return EP_ERR_UNSUPPORTED;
+    if (fp8 && H % 128 != 0)
+        return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (x == nullptr || token_pos == nullptr || !aligned(x, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (num_send > 0 && (recv_x == nullptr || !aligned(recv_x, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (fp8 ? (num_send > 0 && recv_scale == nullptr) : recv_scale != nullptr)
+        return EP_ERR_INVALID_ARG;
+    if (T == 0)
+        return EP_OK;
+    const SendRows rows{token_pos, P};
+    if (fp8)
+        return launch_scatter_fp8(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, recv_scale, err, stream);
+    return launch_scatter_bf16(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, err, stream);
+}
+
+extern "C" int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
+                          int64_t num_send, void *out, int out_dtype, int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!row_shape_ok(T, H) || P < 1 || P > EP_MAX_RANKS || num_send < 0 || num_send >= ((int64_t)1 << 31))
+        return EP_ERR_INVALID_ARG;
+    if (out_dtype != 0 && out_dtype != 1)
+        return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (token_pos == nullptr || out == nullptr || !aligned(out, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (num_send > 0 && (y == nullptr || !aligned(y, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0)
+        return EP_OK;
+    const SendRows rows{token_pos, P};
+    if (out_dtype == 1)
+        return launch_gather<false, true>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err, stream);
+    return launch_gather<false, false>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err, stream);
+}
+
+extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
+                                  int E_local, int rank, int max_num_tokens, void *b_x,
+                                  int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws,
+                                  size_t ws_bytes, int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || E < E_local || E % E_local != 0)
+        return EP_ERR_INVALID_ARG;
+    if (rank < 0 || (int64_t)(rank + 1) * E_local > E || max_num_tokens < 0)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * max_num_tokens >= ((int64_t)1 << 31))
+        return EP_ERR_UNSUPPORTED;
+    if (tokens_per_expert == nullptr || ws == nullptr || !aligned(ws, kWsAlign))
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (x == nullptr || topk_idx == nullptr || slot == nullptr || !aligned(x, 16)))
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * max_num_tokens > 0 && (b_x == nullptr || !aligned(b_x, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (ws_bytes < (size_t)ceil_div(T, kRouteThreads) * E_local * sizeof(int32_t))
+        return EP_ERR_INVALID_ARG;
+
+    int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, max_num_tokens, tokens_per_expert,
+                                  slot, static_cast<int32_t *>(ws), err, stream);
+    if (rc != EP_OK)
+        return rc;
+    if (T > 0) {
+        const BatchedRows rows{topk_idx, slot, nullptr, K, (int64_t)rank * E_local, E_local, max_num_tokens, true};
+        rc = launch_scatter_bf16(x, T, H, rows, (int64_t)E_local * max_num_tokens, EP_ERR_CAPACITY, b_x, err, stream);
+        if (rc != EP_OK)
+            return rc;
+    }
+    if (zero_pad && max_num_tokens > 0) {
+        dim3 grid((unsigned)std::min<int64_t>(ceil_div((int64_t)max_num_tokens * (H / 8), 256), 1024), E_local);
+        zero_pad_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), tokens_per_expert,
+                                                  max_num_tokens, H / 8);
+        return launch_status();
+    }
+    return EP_OK;
+}
+
+extern "C" int ep_batched_combine(const void *y, const int64_t *topk_idx, const float *topk_weights,
+                                  const int32_t *slot, int64_t T, int K, int H, int E_local, int rank,
+                                  int max_num_tokens, void *out, int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || rank < 0 || max_num_tokens < 0)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * max_num_tokens >= ((int64_t)1 << 31))
+        return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (topk_idx == nullptr || topk_weights == nullptr || slot == nullptr || out == nullptr ||
+                  !aligned(out, 16)))
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * max_num_tokens > 0 && (y == nullptr || !aligned(y, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0)
+        return EP_OK;
+    const BatchedRows rows{topk_idx, slot, topk_weights, K, (int64_t)rank * E_local, E_local, max_num_tokens, false};
+    return launch_gather<true, false>(y, T, H, rows, (int64_t)E_local * max_num_tokens, EP_ERR_CAPACITY, out,
+                                      err, stream);
+}
+
+extern "C" int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,
+                                   const float *send_w, int64_t N, int K, int H, void *out, int32_t *err,
+                                   ep_stream_t stream_)
+{
+    (void)err;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (N < 0 || N >= ((int64_t)1 << 31) || K < 1 || K > EP_MAX_TOPK || H < 128 || H % 128 != 0)
+        return EP_ERR_INVALID_ARG;
+    if (N == 0)
+        return EP_OK;
+    if (recv_q == nullptr || recv_scale == nullptr || send_idx == nullptr || send_w == nullptr ||
+        out == nullptr || !aligned(recv_q, 16) || !aligned(out, 16))
+        return EP_ERR_INVALID_ARG;
+    local_expert_fp8_kernel<<<(unsigned)N, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(recv_q),
+                                                             recv_scale, send_idx, send_w, N, K, H,
+                                                             static_cast<uint4 *>(out));
+    return launch_status();
+}

@@ -1,0 +1,542 @@
+// Routing metadata kernels of libep_gb300:
+//   counts  -- axolotl integrations.expert_parallel.torch_dispatch,
+//              compute_send_counts; NeMo uccl_ep.buffer, get_dispatch_layout
+//   layout  -- axolotl build_send_layout (rank-major, token-ascending order)
+//   slots   -- vLLM BatchedPrepareAndFinalize.prepare (per-expert slots that
+//              preserve token order)
+//
+// All three are the same pattern: one thread per token, a warp ballot per
+// destination (rank or local expert) gives each warp's count and every lane's
+// rank among the lanes before it, a shared-memory pass over the block's 8
+// warps gives the block count, and a reduce-then-scan over blocks (partials
+// written to the caller's workspace by one launch, read by the next) gives
+// each block's starting offset.  No atomics decide any position, so every
+// index is deterministic and the order is token-ascending by construction.
+#include <algorithm>
+
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+
+constexpr int kWarps = kRouteThreads / 32;
+
+// ----------------------------------------------------------------- counts --
+__device__ __forceinline__ int chunk_of_block(const ChunkTable &ct, int b)
+{
+    int c = 0;
+    while (c + 1 < ct.n && ct.first_block[c + 1] <= b)
+        ++c;
+    return c;
+}
+
+// One block of 256 tokens (never straddling a chunk): dest, is_in_rank, the
+// block's per-rank token counts and, optionally, its per-expert token counts.
+__global__ void __launch_bounds__(kRouteThreads)
+count_kernel(const int64_t *__restrict__ idx, int K, int P, int E_local, ChunkTable ct,
+             int32_t *__restrict__ dest, uint8_t *__restrict__ is_in_rank,
+             int32_t *__restrict__ part_rank, int32_t *__restrict__ part_expert, int32_t *err)
+{
+    extern __shared__ int32_t smem[];
+    int32_t *warp_cnt = smem;                 // [kWarps][P]
+    int32_t *hist = smem + kWarps * P;        // [E], when part_expert != nullptr
+    const int E = P * E_local;
+    const int b = blockIdx.x;
+    const int c = chunk_of_block(ct, b);
+    const int64_t t = ct.start[c] + (int64_t)(b - ct.first_block[c]) * kRouteThreads + threadIdx.x;
+    const bool valid = t < ct.start[c + 1];
+
+    if (part_expert != nullptr) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            hist[e] = 0;
+        __syncthreads();
+    }
+
+    uint64_t mask = 0;
+    int bad = 0;
+    if (valid) {
+        const int64_t *row = idx + t * K;
+        int32_t *drow = dest + t * K;
+        for (int k = 0; k < K; ++k) {
+            const int64_t id = row[k];
+            int d = -1;
+            if (id >= 0 && id < E)
+                d = (int)(id / E_local);
+            else if (id != -1)
+                bad = EP_ERR_INVALID_EXPERT;
+            drow[k] = d;
+            if (d >= 0) {
+                mask |= 1ull << d;
+                if (part_expert != nullptr) {
+                    bool seen = false;          // count a token once per expert
+                    for (int j = 0; j < k; ++j)
+                        seen |= (row[j] == id);
+                    if (!seen)
+                        atomicAdd(&hist[id], 1);
+                }
+            }
+        }
+        uint8_t *irow = is_in_rank + t * P;
+        for (int p = 0; p < P; ++p)
+            irow[p] = (uint8_t)((mask >> p) & 1ull);
+    }
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int p = 0; p < P; ++p) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+        if (lane == 0)
+            warp_cnt[warp * P + p] = __popc(bal);
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        int s = 0;
+        for (int w = 0; w < kWarps; ++w)
+            s += warp_cnt[w * P + p];
+        part_rank[(int64_t)b * P + p] = s;
+    }
+    if (part_expert != nullptr)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            part_expert[(int64_t)b * E + e] = hist[e];
+    raise(err, bad);
+}
+
+// Single block: per-chunk send_counts and rank_offsets, tokens_per_expert.
+__global__ void __launch_bounds__(1024)
+count_finish_kernel(const int32_t *__restrict__ part_rank, const int32_t *__restrict__ part_expert,
+                    int nb, int P, int E, ChunkTable ct, int32_t *__restrict__ send_counts,
+                    int32_t *__restrict__ rank_offsets, int32_t *__restrict__ tokens_per_expert)
+{
+    for (int i = threadIdx.x; i < ct.n * P; i += blockDim.x) {
+        const int c = i / P, p = i % P;
+        int s = 0;
+        for (int b = ct.first_block[c]; b < ct.first_block[c + 1]; ++b)
+            s += part_rank[(int64_t)b * P + p];
+        send_counts[i] = s;
+    }
+    if (tokens_per_expert != nullptr) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            int s = 0;
+            for (int b = 0; b < nb; ++b)
+                s += part_expert[(int64_t)b * E + e];
+            tokens_per_expert[e] = s;
+        }
+    }
+    if (rank_offsets != nullptr) {
+        __syncthreads();
+        for (int c = threadIdx.x; c < ct.n; c += blockDim.x) {
+            int run = 0;
+            for (int p = 0; p < P; ++p) {
+                rank_offsets[c * (P + 1) + p] = run;
+                run += send_counts[c * P + p];
+            }
+            rank_offsets[c * (P + 1) + P] = run;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- layout --
+__device__ __forceinline__ uint64_t rank_mask(const uint8_t *__restrict__ is_in_rank, int64_t t, int P)
+{
+    uint64_t m = 0;
+    const uint8_t *row = is_in_rank + t * P;
+    for (int p = 0; p < P; ++p)
+        m |= (uint64_t)(row[p] != 0) << p;
+    return m;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+layout_count_kernel(const uint8_t *__restrict__ is_in_rank, int64_t T, int P,
+                    int32_t *__restrict__ part_rank)
+{
+    __shared__ int32_t warp_cnt[kWarps][EP_MAX_RANKS];
+    const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
+    const uint64_t mask = t < T ? rank_mask(is_in_rank, t, P) : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int p = 0; p < P; ++p) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+        if (lane == 0)
+            warp_cnt[warp][p] = __popc(bal);
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        int s = 0;
+        for (int w = 0; w < kWarps; ++w)
+            s += warp_cnt[w][p];
+        part_rank[(int64_t)blockIdx.x * P + p] = s;
+    }
+}
+
+// Exclusive scan over the up-to-64 values held as (v0 for index lane,
+// v1 for index lane+32) by one warp; returns the grand total.
+__device__ __forceinline__ int warp_exclusive_scan64(int v0, int v1, int &e0, int &e1)
+{
+    const int lane = threadIdx.x & 31;
+    int i0 = v0, i1 = v1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n0 = __shfl_up_sync(kFull, i0, off);
+        const int n1 = __shfl_up_sync(kFull, i1, off);
+        if (lane >= off) {
+            i0 += n0;
+            i1 += n1;
+        }
+    }
+    const int s0 = __shfl_sync(kFull, i0, 31);
+    const int s1 = __shfl_sync(kFull, i1, 31);
+    e0 = i0 - v0;
+    e1 = s0 + i1 - v1;
+    return s0 + s1;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+layout_write_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w,
+                    const int32_t *__restrict__ dest, const uint8_t *__restrict__ is_in_rank,
+                    int64_t T, int K, int P, int E_local, int64_t num_send,
+                    const int32_t *__restrict__ part_rank, int nb,
+                    int32_t *__restrict__ send_token_idx, int32_t *__restrict__ send_rank,
+                    int64_t *__restrict__ send_idx, float *__restrict__ send_w,
+                    int32_t *__restrict__ token_pos, int32_t *err)
+{
+    __shared__ int32_t s_base[EP_MAX_RANKS];
+    __shared__ int32_t s_warp[kWarps][EP_MAX_RANKS];
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // This block's first row per rank: all rows of earlier ranks, plus this
+    // rank's rows from earlier blocks.
+    if (warp == 0) {
+        int tot[2] = {0, 0}, before[2] = {0, 0};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = lane + 32 * h;
+            if (p < P)
+                for (int bb = 0; bb < nb; ++bb) {
+                    const int v = part_rank[(int64_t)bb * P + p];
+                    tot[h] += v;
+                    before[h] += bb < b ? v : 0;
+                }
+        }
+        int e0, e1;
+        const int grand = warp_exclusive_scan64(tot[0], tot[1], e0, e1);
+        if (lane < P)
+            s_base[lane] = e0 + before[0];
+        if (lane + 32 < P)
+            s_base[lane + 32] = e1 + before[1];
+        if (b == 0 && lane == 0 && (int64_t)grand != num_send)
+            raise(err, EP_ERR_COUNT_MISMATCH);
+    }
+
+    const int64_t t = (int64_t)b * kRouteThreads + threadIdx.x;
+    const bool valid = t < T;
+    const uint64_t mask = valid ? rank_mask(is_in_rank, t, P) : 0;
+    for (int p = 0; p < P; ++p) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+        if (lane == 0)
+            s_warp[warp][p] = __popc(bal);
+    }
+    __syncthreads();
+    if (threadIdx.x < P) {
+        int run = 0;
+        for (int ww = 0; ww < kWarps; ++ww) {
+            const int v = s_warp[ww][threadIdx.x];
+            s_warp[ww][threadIdx.x] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+
+    int bad = 0;
+    if (valid) {
+        uint64_t dmask = 0;
+        for (int k = 0; k < K; ++k) {
+            const int d = dest[t * K + k];
+            if (d >= 0 && d < P)
+                dmask |= 1ull << d;
+        }
+        if (dmask != mask)
+            bad = EP_ERR_COUNT_MISMATCH;
+    }
+    for (int p = 0; p < P; ++p) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+        if (!valid)
+            continue;
+        int32_t n = -1;
+        if ((mask >> p) & 1ull) {
+            const int64_t pos = (int64_t)s_base[p] + s_warp[warp][p] + __popc(bal & lanemask_lt());
+            if (pos < num_send) {
+                n = (int32_t)pos;
+                send_token_idx[n] = (int32_t)t;
+                send_rank[n] = p;
+                for (int k = 0; k < K; ++k) {
+                    const bool own = dest[t * K + k] == p;
+                    send_idx[(int64_t)n * K + k] = own ? idx[t * K + k] - (int64_t)p * E_local : -1;
+                    send_w[(int64_t)n * K + k] = own ? w[t * K + k] : 0.0f;
+                }
+            } else {
+                bad = EP_ERR_COUNT_MISMATCH;
+            }
+        }
+        token_pos[t * P + p] = n;
+    }
+    raise(err, bad);
+}
+
+// ---------------------------------------------------- expert-batched slots --
+// Local experts are handled 64 at a time (one ballot per expert of the group).
+constexpr int kGroup = 64;
+
+__device__ __forceinline__ uint64_t local_mask(const int64_t *__restrict__ row, int K, int64_t e_lo,
+                                               int n_in_group)
+{
+    uint64_t m = 0;
+    for (int k = 0; k < K; ++k) {
+        const int64_t el = row[k] - e_lo;
+        if (el >= 0 && el < n_in_group)
+            m |= 1ull << el;
+    }
+    return m;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+batched_count_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E, int E_local,
+                     int64_t e0, int32_t *__restrict__ part, int32_t *err)
+{
+    __shared__ int32_t warp_cnt[kWarps][kGroup];
+    const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
+    const bool valid = t < T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int bad = 0;
+    if (valid)
+        for (int k = 0; k < K; ++k) {
+            const int64_t id = idx[t * K + k];
+            if (id < -1 || id >= E)
+                bad = EP_ERR_INVALID_EXPERT;
+        }
+    for (int g0 = 0; g0 < E_local; g0 += kGroup) {
+        const int ng = min(kGroup, E_local - g0);
+        const uint64_t mask = valid ? local_mask(idx + t * K, K, e0 + g0, ng) : 0;
+        for (int e = 0; e < ng; ++e) {
+            const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
+            if (lane == 0)
+                warp_cnt[warp][e] = __popc(bal);
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < ng; e += blockDim.x) {
+            int s = 0;
+            for (int ww = 0; ww < kWarps; ++ww)
+                s += warp_cnt[ww][e];
+            part[(int64_t)blockIdx.x * E_local + g0 + e] = s;
+        }
+        __syncthreads();
+    }
+    raise(err, bad);
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_local, int64_t e0, int M,
+                    const int32_t *__restrict__ part, int nb, int32_t *__restrict__ tokens_per_expert,
+                    int32_t *__restrict__ slot, int32_t *err)
+{
+    __shared__ int32_t s_base[kGroup];
+    __shared__ int32_t s_warp[kWarps][kGroup];
+    const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
+    const bool valid = t < T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int bad = 0;
+    if (valid)
+        for (int k = 0; k < K; ++k)
+            slot[t * K + k] = -1;
+
+    for (int g0 = 0; g0 < E_local; g0 += kGroup) {
+        const int ng = min(kGroup, E_local - g0);
+        if (threadIdx.x < ng) {
+            const int e = g0 + threadIdx.x;
+            int tot = 0, before = 0;
+            for (int bb = 0; bb < nb; ++bb) {
+                const int v = part[(int64_t)bb * E_local + e];
+                tot += v;
+                before += bb < (int)blockIdx.x ? v : 0;
+            }
+            s_base[threadIdx.x] = before;
+            if (blockIdx.x == 0) {
+                tokens_per_expert[e] = min(tot, M);
+                if (tot > M)
+                    bad = EP_ERR_CAPACITY;
+            }
+        }
+        const uint64_t mask = valid ? local_mask(idx + t * K, K, e0 + g0, ng) : 0;
+        for (int e = 0; e < ng; ++e) {
+            const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
+            if (lane == 0)
+                s_warp[warp][e] = __popc(bal);
+        }
+        __syncthreads();
+        if (threadIdx.x < ng) {
+            int run = 0;
+            for (int ww = 0; ww < kWarps; ++ww) {
+                const int v = s_warp[ww][threadIdx.x];
+                s_warp[ww][threadIdx.x] = run;
+                run += v;
+            }
+        }
+        __syncthreads();
+        for (int e = 0; e < ng; ++e) {
+            const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
+            if (!valid || !((mask >> e) & 1ull))
+                continue;
+            const int s = s_base[e] + s_warp[warp][e] + __popc(bal & lanemask_lt());
+            const int32_t v = s < M ? s : -1;
+            if (s >= M)
+                bad = EP_ERR_CAPACITY;
+            for (int k = 0; k < K; ++k)
+                if (idx[t * K + k] == e0 + g0 + e)
+                    slot[t * K + k] = v;
+        }
+        __syncthreads();
+    }
+    raise(err, bad);
+}
+
+int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
+                         int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
+                         int32_t *part, int32_t *err, cudaStream_t stream)
+{
+    const int nb = (int)ceil_div(T, kRouteThreads);
+    const int64_t e0 = (int64_t)rank * E_local;
+    if (nb > 0) {
+        batched_count_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E, E_local, e0, part, err);
+        if (launch_status() != EP_OK)
+            return EP_ERR_CUDA;
+        batched_slot_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E_local, e0, max_num_tokens,
+                                                              part, nb, tokens_per_expert, slot, err);
+        return launch_status();
+    }
+    // T == 0: every expert receives nothing.
+    if (cudaMemsetAsync(tokens_per_expert, 0, sizeof(int32_t) * E_local, stream) != cudaSuccess)
+        return EP_ERR_CUDA;
+    return EP_OK;
+}
+
+}  // namespace ep
+
+// ================================================================ C ABI ====
+using namespace ep;
+
+extern "C" size_t ep_workspace_size(int64_t T, int K, int P, int E_local, int chunks)
+{
+    (void)K;
+    if (T < 0 || P < 1 || E_local < 1)
+        return 0;
+    const int64_t nb = route_blocks_max(T, chunks);
+    const int64_t E = (int64_t)P * E_local;
+    return align_up((size_t)nb * P * sizeof(int32_t), kWsAlign) +
+           align_up((size_t)nb * E * sizeof(int32_t), kWsAlign);
+}
+
+extern "C" int ep_chunk_bounds(int64_t T, int chunks, int64_t *h_bounds)
+{
+    if (T < 0 || chunks < 1 || h_bounds == nullptr)
+        return EP_ERR_INVALID_ARG;
+    const int64_t size = T / chunks;
+    for (int i = 0; i < chunks; ++i)
+        h_bounds[i] = (int64_t)i * size;
+    h_bounds[chunks] = T;
+    return EP_OK;
+}
+
+static bool routing_shape_ok(int64_t T, int K, int P, int E_local)
+{
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || P < 1 || P > EP_MAX_RANKS || E_local < 1)
+        return false;
+    if ((int64_t)P * E_local > EP_MAX_EXPERTS)
+        return false;
+    return T * (int64_t)std::min(K, P) < ((int64_t)1 << 31) && T * (int64_t)K < ((int64_t)1 << 40);
+}
+
+extern "C" int ep_compute_send_counts(const int64_t *topk_idx, int64_t T, int K, int P, int E_local,
+                                      const int64_t *h_chunk_bounds, int chunks, int32_t *dest,
+                                      uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                                      int32_t *tokens_per_expert, void *ws, size_t ws_bytes,
+                                      int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!routing_shape_ok(T, K, P, E_local))
+        return EP_ERR_INVALID_ARG;
+    if (chunks > EP_MAX_CHUNKS)
+        return EP_ERR_UNSUPPORTED;
+    if (send_counts == nullptr || ws == nullptr || !aligned(ws, kWsAlign))
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (topk_idx == nullptr || dest == nullptr || is_in_rank == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (ws_bytes < ep_workspace_size(T, K, P, E_local, chunks))
+        return EP_ERR_INVALID_ARG;
+
+    ChunkTable ct{};
+    const int C = chunks > 1 ? chunks : 1;
+    ct.n = C;
+    if (C > 1) {
+        if (h_chunk_bounds == nullptr || h_chunk_bounds[0] != 0 || h_chunk_bounds[C] != T)
+            return EP_ERR_INVALID_ARG;
+        for (int c = 0; c < C; ++c)
+            if (h_chunk_bounds[c + 1] < h_chunk_bounds[c])
+                return EP_ERR_INVALID_ARG;
+    }
+    int nb = 0;
+    for (int c = 0; c < C; ++c) {
+        ct.start[c] = C > 1 ? h_chunk_bounds[c] : 0;
+        const int64_t end = C > 1 ? h_chunk_bounds[c + 1] : T;
+        ct.first_block[c] = nb;
+        nb += (int)ceil_div(end - ct.start[c], kRouteThreads);
+    }
+    ct.start[C] = T;
+    ct.first_block[C] = nb;
+
+    const int E = P * E_local;
+    const int64_t nb_max = route_blocks_max(T, chunks);
+    int32_t *part_rank = static_cast<int32_t *>(ws);
+    int32_t *part_expert = reinterpret_cast<int32_t *>(
+        static_cast<char *>(ws) + align_up((size_t)nb_max * P * sizeof(int32_t), kWsAlign));
+    int32_t *pe = tokens_per_expert != nullptr ? part_expert : nullptr;
+
+    if (nb > 0) {
+        const size_t smem = sizeof(int32_t) * (kWarps * P + (pe != nullptr ? E : 0));
+        count_kernel<<<nb, kRouteThreads, smem, stream>>>(topk_idx, K, P, E_local, ct, dest, is_in_rank,
+                                                          part_rank, pe, err);
+        if (launch_status() != EP_OK)
+            return EP_ERR_CUDA;
+    }
+    count_finish_kernel<<<1, 1024, 0, stream>>>(part_rank, pe, nb, P, E, ct, send_counts, rank_offsets,
+                                                tokens_per_expert);
+    return launch_status();
+}
+
+extern "C" int ep_build_send_layout(const int64_t *topk_idx, const float *topk_weights,
+                                    const int32_t *dest, const uint8_t *is_in_rank, int64_t T, int K,
+                                    int P, int E_local, int64_t num_send, int32_t *send_token_idx,
+                                    int32_t *send_rank, int64_t *send_idx, float *send_w,
+                                    int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err,
+                                    ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!routing_shape_ok(T, K, P, E_local) || num_send < 0)
+        return EP_ERR_INVALID_ARG;
+    if (ws == nullptr || !aligned(ws, kWsAlign) || ws_bytes < ep_workspace_size(T, K, P, E_local, 1))
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (topk_idx == nullptr || topk_weights == nullptr || dest == nullptr ||
+                  is_in_rank == nullptr || token_pos == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (num_send > 0 && (send_token_idx == nullptr || send_rank == nullptr || send_idx == nullptr ||
+                         send_w == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0)   // nothing is routed: the mismatch, if any, is known on the host
+        return num_send == 0 ? EP_OK : EP_ERR_COUNT_MISMATCH;
+    const int nb = (int)ceil_div(T, kRouteThreads);
+    int32_t *part_rank = static_cast<int32_t *>(ws);
+    layout_count_kernel<<<nb, kRouteThreads, 0, stream>>>(is_in_rank, T, P, part_rank);
+    if (launch_status() != EP_OK)
+        return EP_ERR_CUDA;
+    layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, topk_weights, dest, is_in_rank, T, K, P,
+                                                          E_local, num_send, part_rank, nb, send_token_idx,
+                                                          send_rank, send_idx, send_w, token_pos, err);
+    return launch_status();
+}

@@ -1,0 +1,197 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) MoE top-k token dispatch / combine
+ * library (libep_gb300.so).
+ *
+ * The P destination ranks of expert parallelism are logical partitions of one
+ * GPU's HBM: rank p's receive buffer is the segment [rank_offsets[p],
+ * rank_offsets[p+1]) of one rank-major send buffer, so "sending" is the layout
+ * write itself and no collective runs.
+ *
+ * Citations name the page and the section that define each operation:
+ *   [AX] axolotl docs, integrations.expert_parallel.torch_dispatch
+ *   [UB] NeMo AutoModel docs, nemo_automodel.components.moe.uccl_ep.buffer
+ *   [VB] vLLM docs, vllm.model_executor.layers.fused_moe.prepare_finalize
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless their name starts with h_ (host).
+ *     The caller owns every buffer; the library allocates nothing and keeps no
+ *     state between calls (the "handle" of [AX] TorchEPHandle is token_pos +
+ *     send_counts for the send layout, slot + tokens_per_expert for the
+ *     expert-batched layout).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronises the host.
+ *   - The return value is a status detected on the host (argument checks,
+ *     launch failures): EP_OK, or one EP_ERR_* bit.  On a non-OK return
+ *     nothing was launched by the failing step.
+ *   - Errors found on the device are OR-ed into *err (a device int32 the
+ *     caller zeroes and reads after synchronising; may be NULL).  A kernel that
+ *     finds a bad element skips it and never writes out of bounds.
+ *   - Matrices are row-major and contiguous.  bf16 rows (x, y, recv_x, out)
+ *     must start 16-byte aligned and H must be a multiple of 8.
+ *   - Token, row and count indices are int32 (T * min(K,P) < 2^31); expert ids
+ *     are int64 with -1 meaning "unrouted" ([AX] dispatch, [UB]
+ *     get_dispatch_layout).
+ *   - Limits: 1 <= K <= 32, 1 <= P <= 64, P * E_local <= 8192, chunks <= 64.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *ep_stream_t;
+
+enum ep_status {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,     /* host: null pointer, bad size, misalignment, small workspace */
+    EP_ERR_INVALID_EXPERT = 2,  /* device: a topk id outside [-1, P*E_local); slot treated as unrouted */
+    EP_ERR_COUNT_MISMATCH = 4,  /* device: num_send differs from the routed count, or a row index
+                                   outside [0, num_send), or dest / is_in_rank disagree */
+    EP_ERR_CAPACITY = 8,        /* device: an expert received more than max_num_tokens tokens */
+    EP_ERR_UNSUPPORTED = 16,    /* host: a mode outside the limits (e.g. fp8 with H % 128 != 0) */
+    EP_ERR_CUDA = 32,           /* host: a CUDA launch failed */
+    EP_ERR_TIMEOUT = 64         /* device: a bounded wait gave up */
+};
+
+#define EP_MAX_TOPK 32
+#define EP_MAX_RANKS 64
+#define EP_MAX_EXPERTS 8192
+#define EP_MAX_CHUNKS 64
+
+/* Human-readable name of a status value (a single bit, or EP_OK). */
+const char *ep_status_str(int status);
+
+/* Bytes of device workspace that every workspace-taking call below needs for
+ * these sizes (chunks <= 1 means one chunk).  The workspace must start
+ * 256-byte aligned; its contents need not be initialised and are scratch. */
+size_t ep_workspace_size(int64_t T, int K, int P, int E_local, int chunks);
+
+/* [AX] chunk_bounds (host only): `chunks` contiguous [start, end) token
+ * ranges, h_bounds[i] .. h_bounds[i+1]; every chunk has floor(T / chunks)
+ * tokens and the last takes the remainder, so leading chunks are empty when
+ * T < chunks.  h_bounds has chunks + 1 entries. */
+int ep_chunk_bounds(int64_t T, int chunks, int64_t *h_bounds);
+
+/* [AX] compute_send_counts, [UB] Buffer.get_dispatch_layout.
+ *   topk_idx [T,K] int64: global expert ids, -1 = unrouted.
+ *   Expert e is owned by rank e / E_local.
+ * Outputs:
+ *   dest [T,K] int32: owning rank per slot, -1 where unrouted (or invalid).
+ *   is_in_rank [T,P] uint8: 1 iff some slot of token t is owned by rank p.
+ *   send_counts [C,P] int32, C = max(chunks,1): tokens of chunk c sent to p.
+ *   rank_offsets [C,P+1] int32 or NULL: exclusive prefix of send_counts per
+ *     chunk (rank p's segment of chunk c is [off[c,p], off[c,p+1]) ).
+ *   tokens_per_expert [P*E_local] int32 or NULL: over all T tokens, the
+ *     number of tokens naming expert e in at least one slot.
+ * Chunks: with chunks > 1, h_chunk_bounds (host, chunks+1 entries,
+ * non-decreasing from 0 to T, e.g. from ep_chunk_bounds) splits the tokens,
+ * and all chunks' counts come from this one call ([AX]
+ * dispatch_chunked_forward: one count pass, one device-to-host copy).
+ * Device errors: EP_ERR_INVALID_EXPERT. */
+int ep_compute_send_counts(const int64_t *topk_idx, int64_t T, int K, int P, int E_local,
+                           const int64_t *h_chunk_bounds, int chunks,
+                           int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts,
+                           int32_t *rank_offsets, int32_t *tokens_per_expert,
+                           void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
+/* [AX] build_send_layout (DeepEP layout contract of the [AX] module
+ * description): rank-major, token-ascending send order.  For each rank p in
+ * ascending order and each token t in ascending order with is_in_rank[t,p],
+ * one row n of the send buffer:
+ *   send_token_idx[n] = t, send_rank[n] = p, token_pos[t,p] = n,
+ *   send_idx[n,k] = topk_idx[t,k] - p*E_local if dest[t,k] == p, else -1,
+ *   send_w[n,k]   = topk_weights[t,k]          if dest[t,k] == p, else +0.0f.
+ * token_pos [T,P] int32 is -1 where t is not sent to p; it is the handle that
+ * ep_dispatch and ep_combine take.
+ *   topk_weights [T,K] fp32; dest, is_in_rank from ep_compute_send_counts.
+ *   num_send: host value, the number of rows the caller allocated for
+ *     send_token_idx [N], send_rank [N], send_idx [N,K] int64, send_w [N,K]
+ *     fp32.  It must equal sum(is_in_rank) (passing it from the host avoids
+ *     a device sync, [AX] build_send_layout); a different device count sets
+ *     EP_ERR_COUNT_MISMATCH and rows at or past num_send are not written.
+ * Device errors: EP_ERR_COUNT_MISMATCH. */
+int ep_build_send_layout(const int64_t *topk_idx, const float *topk_weights,
+                         const int32_t *dest, const uint8_t *is_in_rank,
+                         int64_t T, int K, int P, int E_local, int64_t num_send,
+                         int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx,
+                         float *send_w, int32_t *token_pos,
+                         void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
+/* [AX] dispatch on the collective-free local path, [UB] Buffer.dispatch
+ * payloads: recv_x[n] = x[t] for every (t, p) with n = token_pos[t,p] >= 0.
+ * Each source row is read once and written to each of its rows.
+ *   x [T,H] bf16.  token_pos [T,P] from ep_build_send_layout.
+ *   fp8 == 0: recv_x [num_send,H] bf16 (bit copy); recv_scale must be NULL.
+ *   fp8 == 1: recv_x [num_send,H] fp8 e4m3 and recv_scale [num_send,H/128]
+ *     fp32, quantised per token in 1x128 groups: a = max(max|x|, 1e-4),
+ *     q = e4m3_rn_satfinite(x * (448/a)), scale = a/448 (fp32, round to
+ *     nearest even); every row sent for a token carries the same bytes.
+ *     Needs H % 128 == 0.
+ * Device errors: EP_ERR_COUNT_MISMATCH (a token_pos entry >= num_send). */
+int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P,
+                int64_t num_send, void *recv_x, float *recv_scale, int fp8,
+                int32_t *err, ep_stream_t stream);
+
+/* [AX] combine, [UB] Buffer.combine ("addition without weights"): the local
+ * expert kernel has already weighted and summed over K, so
+ *   out[t] = sum over p ascending with token_pos[t,p] >= 0 of y[token_pos[t,p]]
+ * accumulated in fp32 from +0.0f and rounded once; tokens sent nowhere give
+ * +0 ([AX] dispatch: unrouted tokens combine to zero).
+ *   y [num_send,H] bf16.  out [T,H]: bf16 (out_dtype 0) or fp32 (out_dtype 1).
+ * Device errors: EP_ERR_COUNT_MISMATCH (a token_pos entry >= num_send). */
+int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
+               int64_t num_send, void *out, int out_dtype, int32_t *err, ep_stream_t stream);
+
+/* [VB] BatchedPrepareAndFinalize.prepare, unquantised branch: the
+ * expert-batched layout [E_local, max_num_tokens, H].  Local experts are
+ * [rank*E_local, (rank+1)*E_local).  For local expert e_l, the tokens naming
+ * it in some slot, in ascending token order, take slots 0, 1, ...:
+ *   b_x[e_l, s] = x[t],  slot[t,k] = s for every k naming e_l,
+ *   tokens_per_expert[e_l] = number of such tokens (clipped to M).
+ * slot [T,K] int32 is -1 for slots naming non-local experts; it is the handle
+ * of ep_batched_combine.  Rows at or past tokens_per_expert[e_l] are left
+ * untouched unless zero_pad != 0 (then zero-filled, as the page's zero
+ * allocation does).  A token past max_num_tokens is dropped (slot -1, row not
+ * written) and sets EP_ERR_CAPACITY.
+ *   x [T,H] bf16, topk_idx [T,K] int64, E = total experts (E % E_local == 0),
+ *   tokens_per_expert [E_local] int32.
+ * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY. */
+int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H,
+                       int E, int E_local, int rank, int max_num_tokens,
+                       void *b_x, int32_t *tokens_per_expert, int32_t *slot, int zero_pad,
+                       void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
+/* [VB] BatchedPrepareAndFinalize.finalize, [UB] Buffer.low_latency_combine
+ * ("reduce with weights"): this rank's partial
+ *   out[t] = sum over k ascending with a local expert e_l = topk_idx[t,k] -
+ *            rank*E_local and slot[t,k] >= 0 of topk_weights[t,k] * y[e_l, slot[t,k]]
+ * with fp32 fused multiply-add from +0.0f, rounded once to bf16; tokens with
+ * no local expert give +0.  Padding rows of y are never read.
+ *   y [E_local, max_num_tokens, H] bf16, out [T,H] bf16.
+ * Device errors: EP_ERR_CAPACITY (a slot >= max_num_tokens). */
+int ep_batched_combine(const void *y, const int64_t *topk_idx, const float *topk_weights,
+                       const int32_t *slot, int64_t T, int K, int H, int E_local, int rank,
+                       int max_num_tokens, void *out, int32_t *err, ep_stream_t stream);
+
+/* Synthetic local expert kernel for fp8 dispatch workloads (the local_kernel
+ * argument of [AX] dispatch_chunked_forward; the local kernel "weights and
+ * sums over K", [AX] module description).  Expert l maps a token to
+ * dequant(x) * (1 + l/64) in bf16:
+ *   d = e4m3(q) * scale,  y_k = bf16(d * (1 + l_k/64)) for send_idx[n,k] = l_k >= 0,
+ *   out[n] = bf16(fma over k ascending of send_w[n,k] * y_k, from +0.0f).
+ *   recv_q [N,H] e4m3, recv_scale [N,H/128] fp32, send_idx [N,K] int64,
+ *   send_w [N,K] fp32, out [N,H] bf16.  H % 128 == 0. */
+int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,
+                        const float *send_w, int64_t N, int K, int H, void *out,
+                        int32_t *err, ep_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

@@ -1,0 +1,67 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/ep.h declares; host-side argument checks answer without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_send_counts_gb300 as ep
+from combine_send_counts_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ep.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ep_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ctypes.CDLL(_build.LIB_PATH)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ep_compute_send_counts", "ep_build_send_layout", "ep_dispatch", "ep_combine",
+                     "ep_batched_prepare", "ep_batched_combine", "ep_chunk_bounds", "ep_workspace_size",
+                     "ep_status_str", "ep_local_expert_fp8"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    for n in declared_functions():
+        assert callable(getattr(ep, n, None)), n
+
+
+def test_host_only_calls(lib):
+    assert ep.ep_status_str(0) == "EP_OK"
+    assert ep.ep_status_str(ep.EP_ERR_CAPACITY) == "EP_ERR_CAPACITY"
+    assert ep.ep_chunk_bounds(10, 3) == [0, 3, 6, 10]
+    assert ep.ep_chunk_bounds(2, 4) == [0, 0, 0, 0, 2]
+    assert ep.ep_workspace_size(16384, 8, 8, 32, 1) > 0
+    with pytest.raises(ep.EPError):
+        ep.ep_chunk_bounds(5, 0)
+
+
+def test_argument_checks_reject_before_launch(lib):
+    # Null / impossible arguments are rejected on the host: no device is touched.
+    vp = ctypes.c_void_p
+    lib.ep_dispatch.argtypes = [vp, ctypes.c_int64, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int64, vp, vp,
+                                ctypes.c_int, vp, vp]
+    assert lib.ep_dispatch(None, 4, 7, None, 2, 4, None, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # H % 8
+    assert lib.ep_dispatch(None, 4, 64, None, 2, 4, None, None, 1, None, None) == ep.EP_ERR_UNSUPPORTED  # fp8, H % 128
+    assert lib.ep_dispatch(None, 4, 64, None, 0, 4, None, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # P = 0
+    assert lib.ep_dispatch(None, 0, 64, None, 2, 0, None, None, 0, None, None) == ep.EP_OK  # empty: nothing to do
+    lib.ep_combine.argtypes = [vp, ctypes.c_int64, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int64, vp,
+                               ctypes.c_int, vp, vp]
+    assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 2, None, None) == ep.EP_ERR_UNSUPPORTED  # out_dtype
+    assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # null out

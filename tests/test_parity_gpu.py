@@ -1,0 +1,325 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.  Counts, layouts, indices and moved bytes are
+compared bit for bit; combine outputs too (both sides accumulate in fp32 in
+the same order with the same roundings, which is stricter than the 1 bf16 ulp
+target).  Full-size workloads run at the sizes the benchmark times."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import combine_send_counts_gb300 as ep
+import oracle
+from combine_send_counts_gb300 import workloads as wl
+
+from _paths import (assert_combine_parity, assert_equal, bits16, compare_send_path, gpu_send_path, np_)
+
+pytestmark = pytest.mark.gpu
+
+
+def _send_inputs(w: wl.Workload):
+    x, idx, wts = wl.make(w)
+    return x, idx, wts
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "large"])
+def test_send_path_workload(name):
+    w = wl.WORKLOADS[name]
+    x, idx, wts = _send_inputs(w)
+    o = oracle.send_path(x, idx, wts, None, w.P, w.E_local)
+    y = wl.expert_outputs(w, o["layout"]["n"])
+    o["out"] = oracle.combine(y, o["layout"]["token_pos"])
+    g = gpu_send_path(x, idx, wts, y, w.P, w.E_local)
+    compare_send_path(x, idx, wts, y, w.P, w.E_local, g, o)
+
+
+def test_send_path_fp32_combine():
+    w = wl.WORKLOADS["mid"]
+    x, idx, wts = _send_inputs(w)
+    o = oracle.send_path(x, idx, wts, None, w.P, w.E_local)
+    y = wl.expert_outputs(w, o["layout"]["n"])
+    want = oracle.combine(y, o["layout"]["token_pos"], out_f32=True)
+    g = gpu_send_path(x, idx, wts, y, w.P, w.E_local, out_f32=True)
+    assert_equal("combine fp32 (bits)", np_(g["out"]).view(np.uint32), want.view(np.uint32))
+
+
+def _batched(w: wl.Workload, zero_pad=False):
+    x, idx, wts = wl.make(w)
+    o = oracle.batched_prepare(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, zero_pad=zero_pad)
+    dev = "cuda"
+    r = ep.batched_prepare(x.to(dev), idx.to(dev), w.E, w.E_local, w.rank, w.max_num_tokens, zero_pad=zero_pad)
+    y = wl.batched_expert_outputs(w, o["tokens_per_expert"])
+    o_out = oracle.batched_combine(y, idx, wts, o["slot"], w.E_local, w.rank)
+    g_out = ep.batched_combine(y.to(dev), idx.to(dev), wts.to(dev), r["slot"], w.rank, err=r["err"])
+    torch.cuda.synchronize()
+    return x, idx, wts, o, r, o_out, g_out
+
+
+def test_batched_workload():
+    w = wl.WORKLOADS["batched"]
+    x, idx, wts, o, r, o_out, g_out = _batched(w)
+    assert int(r["err"].item()) == 0
+    tpe = o["tokens_per_expert"]
+    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), tpe)
+    assert_equal("slot", np_(r["slot"]), o["slot"])
+    bx = bits16(r["b_x"])
+    for e in range(w.E_local):
+        assert_equal(f"b_x[{e}] valid rows", bx[e, :tpe[e]], o["b_x"][e, :tpe[e]])
+    out_bits = bits16(g_out)
+    assert not np.any(np.isnan(g_out.float().cpu().numpy())), "combine read a NaN padding row"
+    assert_combine_parity("batched combine", out_bits, o_out)
+
+
+def test_batched_zero_pad_small():
+    w = dataclasses.replace(wl.WORKLOADS["batched"].scaled(T=1000), max_num_tokens=300, H=264)
+    x, idx, wts, o, r, o_out, g_out = _batched(w, zero_pad=True)
+    assert int(r["err"].item()) == 0
+    assert_equal("b_x (zero padded)", bits16(r["b_x"]), o["b_x"])
+    assert_combine_parity("batched combine", bits16(g_out), o_out)
+
+
+def _chunked_fp8(w: wl.Workload):
+    """One count launch for all chunks, one D2H of the counts, then per chunk
+    layout -> fp8 dispatch -> synthetic expert -> combine on the GPU."""
+    dev = "cuda"
+    x, idx, wts = wl.make(w)
+    bounds = ep.chunk_bounds(w.T, w.chunks)
+    xd, idd, wd = x.to(dev), idx.to(dev), wts.to(dev)
+    err = ep.error_word()
+    c = ep.compute_send_counts(idd, w.P, w.E_local, chunk_bounds=bounds, err=err)
+    counts = c["send_counts"].cpu()                       # the one device-to-host copy
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    per_chunk = []
+    for i in range(w.chunks):
+        s, e = bounds[i], bounds[i + 1]
+        N = int(counts[i].sum())
+        lay = ep.build_send_layout(idd[s:e], wd[s:e], c["dest"][s:e], c["is_in_rank"][s:e], N, w.E_local, err=err)
+        q, sc = ep.dispatch_rows(xd[s:e], lay["token_pos"], N, fp8=True, err=err)
+        local = ep.local_expert_fp8(q, sc, lay["send_idx"], lay["send_w"], err=err)
+        out[s:e] = ep.combine_rows(local, lay["token_pos"], err=err)
+        per_chunk.append(dict(layout=lay, q=q, scale=sc, local=local, N=N))
+    torch.cuda.synchronize()
+    return x, idx, wts, bounds, c, per_chunk, out, int(err.item())
+
+
+def test_chunked_fp8_reduced_full_compare():
+    w = wl.WORKLOADS["chunk_fp8"].scaled(T=2048 + 37)    # 4 ragged chunks
+    x, idx, wts, bounds, c, per_chunk, out, err = _chunked_fp8(w)
+    assert err == 0
+    assert bounds == oracle.chunk_bounds(w.T, w.chunks).tolist()
+    ob = oracle.chunk_bounds(w.T, w.chunks)
+    for i in range(w.chunks):
+        s, e = int(ob[i]), int(ob[i + 1])
+        oc = oracle.compute_send_counts(idx[s:e], w.P, w.E_local)
+        assert_equal(f"chunk {i} send_counts", np_(c["send_counts"][i]), oc["send_counts"])
+        ol = oracle.build_send_layout(idx[s:e], wts[s:e], oc["dest"], oc["is_in_rank"], w.E_local)
+        g = per_chunk[i]
+        for k in ("send_token_idx", "send_rank", "send_idx", "token_pos"):
+            assert_equal(f"chunk {i} {k}", np_(g["layout"][k]), ol[k])
+        q, sc = oracle.dispatch_fp8(x[s:e], ol["send_token_idx"])
+        assert_equal(f"chunk {i} fp8 codes", np_(g["q"]), q)
+        assert_equal(f"chunk {i} fp8 scales (bits)", np_(g["scale"]).view(np.uint32), sc.view(np.uint32))
+        local = oracle.local_expert_fp8(q, sc, ol["send_idx"], ol["send_w"])
+        assert_equal(f"chunk {i} local expert", bits16(g["local"]), local)
+        o_out = oracle.combine(local, ol["token_pos"])
+        assert_combine_parity(f"chunk {i} combine", bits16(out[s:e]), o_out)
+    # tokens_per_expert over all chunks from the same single count launch
+    assert_equal("tokens_per_expert", np_(c["tokens_per_expert"]),
+                 oracle.compute_send_counts(idx, w.P, w.E_local)["tokens_per_expert"])
+
+
+def test_chunked_fp8_full_size_sampled():
+    w = wl.WORKLOADS["chunk_fp8"]
+    x, idx, wts, bounds, c, per_chunk, out, err = _chunked_fp8(w)
+    assert err == 0
+    # counts of every chunk, exactly (integer work, cheap on the host)
+    for i in range(w.chunks):
+        s, e = bounds[i], bounds[i + 1]
+        oc = oracle.compute_send_counts(idx[s:e], w.P, w.E_local, with_tokens_per_expert=False)
+        assert_equal(f"chunk {i} send_counts", np_(c["send_counts"][i]), oc["send_counts"])
+    # sampled tokens: the whole pipeline for one token is the pipeline on the
+    # one-token problem (each token's result depends only on its own row,
+    # routing and weights)
+    g = np.random.Generator(np.random.PCG64(123))
+    sample = np.sort(g.choice(w.T, size=96, replace=False))
+    outb = bits16(out)
+    for t in sample.tolist():
+        xi, ii, wi = x[t:t + 1], idx[t:t + 1], wts[t:t + 1]
+        r = oracle.send_path(xi, ii, wi, None, w.P, w.E_local)
+        lay = r["layout"]
+        q, sc = oracle.dispatch_fp8(xi, lay["send_token_idx"])
+        local = oracle.local_expert_fp8(q, sc, lay["send_idx"], lay["send_w"])
+        want = oracle.combine(local, lay["token_pos"])
+        assert_combine_parity(f"token {t}", outb[t:t + 1], want)
+
+
+def test_fp8_codes_for_every_bf16_input():
+    # Groups whose max is exactly 448 have inv = 448/448 = 1, so the codes are
+    # the plain e4m3 conversion of every finite bf16 value with |x| <= 448.
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = oracle.bf16_bits_to_f32(allb)
+    vals = allb[np.isfinite(f) & (np.abs(f) <= 448.0)]
+    per = 127
+    ngroups = -(-vals.size // per)
+    H = 128 * 16
+    rows = -(-ngroups // 16)
+    buf = np.zeros((rows * 16, 128), np.uint16)
+    buf[:, 0] = 0x43E0                                    # 448.0 in bf16
+    flat = np.zeros(rows * 16 * per, np.uint16)
+    flat[:vals.size] = vals
+    buf[:, 1:] = flat.reshape(rows * 16, per)
+    x = torch.from_numpy(buf.reshape(rows, H).view(np.int16)).view(torch.bfloat16)
+    T = rows
+    token_pos = torch.arange(T, dtype=torch.int32).view(T, 1)
+    err = ep.error_word()
+    q, s = ep.dispatch_rows(x.cuda(), token_pos.cuda(), T, fp8=True, err=err)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quantize_fp8_rows(x)
+    assert int(err.item()) == 0
+    assert_equal("codes", np_(q), oq)
+    assert np.all(np_(s) == np.float32(1.0))
+    assert_equal("scales", np_(s), os_)
+
+
+# ------------------------------------------------------------------ edges --
+def _routing(T, K, E, seed, frac_unrouted=0.1, dup=False):
+    g = np.random.Generator(np.random.PCG64(seed))
+    idx = (g.integers(0, E, size=(T, K)) if dup else np.argsort(g.random((T, E)), 1)[:, :K]).astype(np.int64)
+    idx[g.random((T, K)) < frac_unrouted] = -1
+    w = g.random((T, K)).astype(np.float32)
+    w[idx < 0] = 0
+    return torch.from_numpy(idx), torch.from_numpy(w)
+
+
+def _randn(T, H, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    return torch.from_numpy(g.standard_normal((T, H), dtype=np.float32)).to(torch.bfloat16)
+
+
+EDGE = [
+    # T, H, K, P, E_local, frac_unrouted, dup
+    (1, 64, 2, 4, 2, 0.0, False),
+    (1000, 136, 4, 8, 4, 0.1, False),        # ragged tokens and a ragged vector count
+    (257, 8, 3, 2, 3, 0.3, True),            # smallest row, duplicate experts
+    (600, 256, 8, 1, 16, 0.2, False),        # P = 1
+    (300, 128, 32, 64, 1, 0.05, False),      # K = 32, P = 64
+    (777, 512, 1, 16, 4, 0.25, False),       # K = 1: counting sort
+    (513, 1024, 6, 8, 8, 1.0, False),        # nothing routed
+    (300, 16384, 4, 4, 4, 0.0, False),       # a row longer than one pass of the block
+]
+
+
+@pytest.mark.parametrize("T,H,K,P,E_local,fu,dup", EDGE)
+def test_send_path_edges(T, H, K, P, E_local, fu, dup):
+    idx, wts = _routing(T, K, P * E_local, seed=T + H, frac_unrouted=fu, dup=dup)
+    x = _randn(T, H, T)
+    o = oracle.send_path(x, idx, wts, None, P, E_local)
+    y = _randn(max(o["layout"]["n"], 1), H, T + 1)[:o["layout"]["n"]]
+    o["out"] = oracle.combine(y, o["layout"]["token_pos"])
+    g = gpu_send_path(x, idx, wts, y, P, E_local)
+    compare_send_path(x, idx, wts, y, P, E_local, g, o)
+
+
+def test_empty_inputs():
+    dev = "cuda"
+    idx = torch.empty((0, 4), dtype=torch.int64, device=dev)
+    c = ep.compute_send_counts(idx, 4, 2)
+    torch.cuda.synchronize()
+    assert np_(c["send_counts"]).tolist() == [[0, 0, 0, 0]]
+    assert np_(c["rank_offsets"]).tolist() == [[0, 0, 0, 0, 0]]
+    assert np_(c["tokens_per_expert"]).tolist() == [0] * 8
+    lay = ep.build_send_layout(idx, torch.empty((0, 4), device=dev), c["dest"], c["is_in_rank"], 0, 2)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
+    assert ep.dispatch_rows(x, lay["token_pos"], 0).shape == (0, 64)
+    assert ep.combine_rows(torch.empty((0, 64), dtype=torch.bfloat16, device=dev), lay["token_pos"]).shape == (0, 64)
+    r = ep.batched_prepare(x, idx, 8, 2, 1, 16)
+    torch.cuda.synchronize()
+    assert np_(r["tokens_per_expert"]).tolist() == [0, 0]
+    with pytest.raises(ep.EPError):
+        ep.build_send_layout(idx, torch.empty((0, 4), device=dev), c["dest"], c["is_in_rank"], 3, 2)
+
+
+def test_invalid_expert_ids_are_flagged_and_skipped():
+    idx = torch.tensor([[0, 99], [-7, 3], [5, -1], [2, 1]], dtype=torch.int64)
+    wts = torch.full((4, 2), 0.5)
+    x = _randn(4, 64, 5)
+    o = oracle.send_path(x, idx, wts, None, 4, 2)
+    assert o["counts"]["err"] & oracle.ERR_INVALID_EXPERT
+    y = _randn(o["layout"]["n"], 64, 6)
+    o["out"] = oracle.combine(y, o["layout"]["token_pos"])
+    g = gpu_send_path(x, idx, wts, y, 4, 2)
+    assert g["err"] & ep.EP_ERR_INVALID_EXPERT
+    g["err"] = 0
+    compare_send_path(x, idx, wts, y, 4, 2, g, o)
+
+
+def test_num_send_mismatch_is_flagged_and_writes_stay_in_bounds():
+    T, H, K, P, El = 500, 64, 4, 4, 4
+    idx, wts = _routing(T, K, P * El, 3)
+    dev = "cuda"
+    c = ep.compute_send_counts(idx.to(dev), P, El)
+    N = int(c["send_counts"].sum().item())
+    short = N - 7
+    guard = 16
+    err = ep.error_word()
+    sti = torch.full((short + guard,), -12345, dtype=torch.int32, device=dev)
+    sr = torch.full_like(sti, -12345)
+    si = torch.full(((short + guard), K), -12345, dtype=torch.int64, device=dev)
+    sw = torch.full(((short + guard), K), 7.0, dtype=torch.float32, device=dev)
+    tp = torch.empty((T, P), dtype=torch.int32, device=dev)
+    ws = ep.workspace(T, K, P, El)
+    ep.ep_build_send_layout(idx.to(dev), wts.to(dev), c["dest"], c["is_in_rank"], T, K, P, El, short,
+                            sti, sr, si, sw, tp, ws, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ep.EP_ERR_COUNT_MISMATCH
+    assert np.all(np_(sti[short:]) == -12345) and np.all(np_(si[short:]) == -12345)
+    assert np.all(np_(sw[short:]) == 7.0)
+    assert int(tp.max().item()) < short
+    # dispatch with the clipped handle writes only rows < short
+    x = _randn(T, H, 4).to(dev)
+    recv = torch.full((short + guard, H), 3.0, dtype=torch.bfloat16, device=dev)
+    ep.ep_dispatch(x, T, H, tp, P, short, recv, None, 0, err)
+    torch.cuda.synchronize()
+    assert torch.all(recv[short:] == 3.0)
+
+
+def test_batched_capacity_overflow():
+    T, H, K, E, El, rank, M = 400, 64, 4, 8, 4, 0, 50
+    idx, wts = _routing(T, K, E, 8, frac_unrouted=0.0)
+    x = _randn(T, H, 9)
+    o = oracle.batched_prepare(x, idx, E, El, rank, M)
+    assert o["err"] & oracle.ERR_CAPACITY
+    dev = "cuda"
+    guard = torch.full((El * M + 8, H), 5.0, dtype=torch.bfloat16, device=dev)
+    b_x = guard[:El * M].view(El, M, H)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    err = ep.error_word()
+    ws = ep.workspace(T, K, E // El, El)
+    ep.ep_batched_prepare(x.to(dev), idx.to(dev), T, K, H, E, El, rank, M, b_x, tpe, slot, 0, ws, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ep.EP_ERR_CAPACITY
+    assert_equal("tokens_per_expert (clipped)", np_(tpe), o["tokens_per_expert"])
+    assert_equal("slot", np_(slot), o["slot"])
+    assert torch.all(guard[El * M:] == 5.0)
+    bx = bits16(b_x)
+    for e in range(El):
+        assert_equal(f"b_x[{e}]", bx[e, :o["tokens_per_expert"][e]], o["b_x"][e, :o["tokens_per_expert"][e]])
+
+
+def test_batched_duplicate_experts_small():
+    T, H, K, E, El, rank, M = 333, 128, 6, 12, 4, 2, 400
+    idx, wts = _routing(T, K, E, 10, dup=True)
+    x = _randn(T, H, 11)
+    o = oracle.batched_prepare(x, idx, E, El, rank, M)
+    dev = "cuda"
+    r = ep.batched_prepare(x.to(dev), idx.to(dev), E, El, rank, M)
+    w = wl.Workload("dup", T=T, H=H, E=E, K=K, P=E // El, routing="uniform", rank=rank, max_num_tokens=M)
+    y = wl.batched_expert_outputs(w, o["tokens_per_expert"])
+    o_out = oracle.batched_combine(y, idx, wts, o["slot"], El, rank)
+    g_out = ep.batched_combine(y.to(dev), idx.to(dev), wts.to(dev), r["slot"], rank, err=r["err"])
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    assert_equal("slot", np_(r["slot"]), o["slot"])
+    assert_combine_parity("batched combine", bits16(g_out), o_out)
