@@ -66,6 +66,8 @@ _SIGNATURES = {
                                   _VP, _SZ, _VP, _VP]),
     "ep_batched_combine": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
     "ep_local_expert_fp8": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP]),
+    "ep_compute_send_counts_noalloc": (_I32, [_VP, _I64, _I32, _I32, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
+                                              _VP, _VP]),
 }
 
 
@@ -182,6 +184,20 @@ def ep_local_expert_fp8(recv_q, recv_scale, send_idx, send_w, N, K, H, out, err,
     rc = load().ep_local_expert_fp8(_p(recv_q), _p(recv_scale), _p(send_idx), _p(send_w), int(N), int(K),
                                     int(H), _p(out), _p(err), _stream(stream))
     _check(rc, "ep_local_expert_fp8")
+
+
+def ep_compute_send_counts_noalloc(topk_idx, T, K, P, E_local, h_chunk_bounds, chunks, dest, is_in_rank,
+                                   send_counts, rank_offsets, tokens_per_expert, err, stream=None):
+    """ep_compute_send_counts without a workspace argument: for callers that
+    cannot allocate device memory, the library's own fixed device array holds
+    the scratch (include/ep.h states its size limit and sharing rules)."""
+    hb = None
+    if h_chunk_bounds is not None:
+        hb = (ctypes.c_int64 * len(h_chunk_bounds))(*[int(v) for v in h_chunk_bounds])
+    rc = load().ep_compute_send_counts_noalloc(_p(topk_idx), int(T), int(K), int(P), int(E_local), hb,
+                                               int(chunks), _p(dest), _p(is_in_rank), _p(send_counts),
+                                               _p(rank_offsets), _p(tokens_per_expert), _p(err), _stream(stream))
+    _check(rc, "ep_compute_send_counts_noalloc")
 
 
 # ------------------------------------------------------------------ helpers --

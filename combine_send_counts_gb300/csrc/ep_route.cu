@@ -540,3 +540,69 @@ extern "C" int ep_build_send_layout(const int64_t *topk_idx, const float *topk_w
                                                           send_rank, send_idx, send_w, token_pos, err);
     return launch_status();
 }
+
+// ====================================================== no-allocation variant ==
+// ep_compute_send_counts_noalloc: the same counts, with the per-block partial
+// counts kept in a fixed device array that the library holds, so the caller
+// passes no workspace.  It exists for callers that cannot allocate device
+// memory themselves: engines that plan all device memory before they start
+// and forbid allocation while they run (for example inside a plugin's enqueue
+// step), and code that must not call cudaMalloc while a CUDA graph is being
+// captured.
+//
+// The array below is set up once per device: the first call on a device
+// (with that device current) looks up its device address with
+// cudaGetSymbolAddress and caches it.  Every call on a device shares the one
+// array, which keeps the last call's contents; the count kernels overwrite
+// every partial they read, so nothing needs clearing between calls.  Calls
+// whose kernels overlap on the GPU (other streams, other host threads) race
+// on the array.
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_count_scratch[EP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_count_scratch on the current device.  Host code cannot
+// use the symbol itself: on the host it names a stand-in, not device memory.
+int count_scratch_address(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return EP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_count_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return EP_OK;
+}
+}  // namespace
+
+extern "C" int ep_compute_send_counts_noalloc(const int64_t *topk_idx, int64_t T, int K, int P, int E_local,
+                                              const int64_t *h_chunk_bounds, int chunks, int32_t *dest,
+                                              uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                                              int32_t *tokens_per_expert, int32_t *err, ep_stream_t stream)
+{
+    if (ep_workspace_size(T, K, P, E_local, chunks) > (size_t)EP_NOALLOC_SCRATCH_BYTES)
+        return EP_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    const int rc = count_scratch_address(&scratch);
+    if (rc != EP_OK)
+        return rc;
+    return ep_compute_send_counts(topk_idx, T, K, P, E_local, h_chunk_bounds, chunks, dest, is_in_rank,
+                                  send_counts, rank_offsets, tokens_per_expert, scratch,
+                                  (size_t)EP_NOALLOC_SCRATCH_BYTES, err, stream);
+}

@@ -190,6 +190,33 @@ int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const in
                         const float *send_w, int64_t N, int K, int H, void *out,
                         int32_t *err, ep_stream_t stream);
 
+/* Same as ep_compute_send_counts, but the caller passes no workspace: the
+ * scratch lives in one fixed device array of EP_NOALLOC_SCRATCH_BYTES that the
+ * library holds on every device that loads it, until the process exits.  The
+ * pages have no counterpart of this call; it is for callers that cannot
+ * allocate device memory themselves, such as engines that plan all device
+ * memory up front and forbid allocation while they run (a plugin's enqueue
+ * step), or code that must not call cudaMalloc while a CUDA graph is being
+ * captured.
+ *   - Sizes whose workspace (ep_workspace_size) exceeds
+ *     EP_NOALLOC_SCRATCH_BYTES are rejected with EP_ERR_UNSUPPORTED before
+ *     anything is launched (1 MiB covers e.g. T = 65536, P = 16, E = 256).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture begins.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose kernels
+ *     overlap on the GPU -- on other streams or from other host threads --
+ *     race on it; serialise them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define EP_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+int ep_compute_send_counts_noalloc(const int64_t *topk_idx, int64_t T, int K, int P, int E_local,
+                                   const int64_t *h_chunk_bounds, int chunks,
+                                   int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts,
+                                   int32_t *rank_offsets, int32_t *tokens_per_expert,
+                                   int32_t *err, ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
