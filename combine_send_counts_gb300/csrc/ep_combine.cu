@@ -1,0 +1,396 @@
+// Combine kernels of libep_gb300:
+//   ep_combine          -- axolotl integrations.expert_parallel.torch_dispatch,
+//                          combine; NeMo uccl_ep.buffer, Buffer.combine
+//                          (addition without weights)
+//   ep_batched_combine  -- vLLM BatchedPrepareAndFinalize.finalize; NeMo
+//                          uccl_ep.buffer, Buffer.low_latency_combine (reduce
+//                          with weights)
+//
+// Both read, for every output token, its source rows in a fixed order and
+// accumulate them in fp32.  The work is HBM-bound and its rows are scattered,
+// so the kernel keeps many row loads in flight with the TMA engine rather
+// than with registers:
+//
+//   * one persistent CTA per SM; items are (token, column chunk) pairs, dealt
+//     round-robin over the CTAs;
+//   * warp 0 is the producer: it resolves the source lists of 32 items at a
+//     time, publishes each item's descriptor (token, chunk, source count,
+//     weights) in a small queue and issues one 1-D bulk copy
+//     (cp.async.bulk, global -> shared) per source row chunk into a ring of
+//     B shared-memory buffers, each tracked by a "full" mbarrier (transaction
+//     bytes) and an "empty" mbarrier (consumer warps' release);
+//   * warps 1..8 are consumers: they take the items in the same order, wait
+//     for each source buffer, accumulate it into fp32 registers (16 bytes of
+//     the row per thread and pass), release the buffer and write the output
+//     chunk once with 16-byte streaming stores.
+//
+// Every wait is bounded (EP_ERR_TIMEOUT after a second); a CTA that gives up
+// waits, again with a bound, for its own copies in flight before it exits.
+#include <algorithm>
+
+#include "ep_device.cuh"
+#include "ep_internal.h"
+#include "ep_rows.cuh"
+
+namespace ep {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kGatherThreads = 32 + kConsumers;
+constexpr int kQueue = 16;          // descriptor slots: how far the producer may run ahead in items
+constexpr int kBatch = 32;          // items whose source lists the producer resolves at once
+constexpr int kVMax = 4;            // 16-byte vectors per consumer thread per chunk
+constexpr int kMaxChunkCols = kConsumers * kVMax * 8;   // 8192 bf16 columns = 16 KB per buffer
+constexpr int kMaxBuffers = 64;
+constexpr size_t kSmemBudget = 210 * 1024;
+constexpr uint64_t kWaitNs = 1000000000ull;       // 1 s
+constexpr uint64_t kDrainNs = 50000000ull;        // 50 ms per buffer when draining after a timeout
+
+struct Desc {
+    int64_t t;
+    int32_t c;
+    int32_t nsrc;
+    float w[kMaxList];
+};
+
+struct GatherGeom {
+    int H;          // columns per row
+    int CH;         // columns per chunk (multiple of 8)
+    int nchunk;     // chunks per row
+    int B;          // ring buffers, a power of two
+    int logB;       // log2(B): buffer of use u is u & (B-1), its phase parity (u >> logB) & 1
+    int RB;         // bytes per ring buffer (multiple of 128)
+};
+
+__host__ __device__ inline size_t gather_smem_bytes(const GatherGeom &g, int D)
+{
+    return (size_t)g.B * g.RB                       // ring
+           + sizeof(uint64_t) * (2 * g.B + 2 * kQueue)   // mbarriers
+           + sizeof(int64_t) * g.B                   // last armed use per buffer
+           + sizeof(Desc) * kQueue                   // descriptor queue
+           + (sizeof(int32_t) + sizeof(float)) * kBatch * D + sizeof(int32_t) * kBatch;   // lists
+}
+
+template <class Rows, bool WEIGHTED, bool OUT_F32>
+__global__ void __launch_bounds__(kGatherThreads, 1)
+gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows rows, int64_t n_rows,
+                  int err_bits, void *__restrict__ out, int32_t *err)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int D = rows.len();
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)g.B * g.RB);
+    uint64_t *empty = full + g.B;
+    uint64_t *qfull = empty + g.B;
+    uint64_t *qempty = qfull + kQueue;
+    int64_t *last_use = reinterpret_cast<int64_t *>(qempty + kQueue);
+    Desc *desc = reinterpret_cast<Desc *>(last_use + g.B);
+    int32_t *l_row = reinterpret_cast<int32_t *>(desc + kQueue);
+    float *l_w = reinterpret_cast<float *>(l_row + kBatch * D);
+    int32_t *l_n = reinterpret_cast<int32_t *>(l_w + kBatch * D);
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < g.B; ++b) {
+            mbar_init(&full[b], 1);
+            mbar_init(&empty[b], kConsumerWarps);
+            last_use[b] = -1;
+        }
+        for (int q = 0; q < kQueue; ++q) {
+            mbar_init(&qfull[q], 1);
+            mbar_init(&qempty[q], kConsumerWarps);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    volatile int *abort_flag = &s_abort;
+    const int n_items = (int)(T * g.nchunk);   // < 2^31, checked on the host
+    const int stride = gridDim.x;
+    int bad = 0;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        uint32_t use = 0;  // buffer uses armed so far (warp-uniform)
+        uint32_t k = 0;    // items published so far
+        for (int i0 = blockIdx.x; i0 < n_items && !*abort_flag; i0 += stride * kBatch) {
+            // lane l resolves the source list of item i0 + l * stride
+            const int mine = i0 + lane * stride;
+            int n = 0;
+            if (mine < n_items) {
+                const int64_t t = g.nchunk == 1 ? mine : mine / g.nchunk;
+                for (int j0 = 0; j0 < D; j0 += 8) {
+                    int32_t r8[8];
+                    float w8[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = j0 + jj;
+                        r8[jj] = j < D ? rows.row(t, j) : -1;
+                        w8[jj] = (WEIGHTED && j < D) ? rows.weight(t, j) : 1.0f;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        int32_t r = r8[jj];
+                        if (r >= n_rows) {
+                            bad = err_bits;
+                            r = -1;
+                        }
+                        if (r >= 0) {
+                            l_row[lane * D + n] = r;
+                            l_w[lane * D + n] = w8[jj];
+                            ++n;
+                        }
+                    }
+                }
+            }
+            l_n[lane] = n;
+            __syncwarp();
+            const int left = (n_items - i0 + stride - 1) / stride;
+            const int nb = left < kBatch ? left : kBatch;
+            for (int bi = 0; bi < nb; ++bi, ++k) {
+                const int item = i0 + bi * stride;
+                const int nsrc = l_n[bi];
+                const int q = (int)(k % kQueue);
+                bool ok = true;
+                if (lane == 0 && k >= kQueue)
+                    ok = mbar_wait(&qempty[q], ((k / kQueue) - 1) & 1, kWaitNs);
+                if (!__all_sync(kFull, ok)) {
+                    bad |= EP_ERR_TIMEOUT;
+                    *abort_flag = 1;
+                    break;
+                }
+                const int chunk = g.nchunk == 1 ? 0 : item % g.nchunk;
+                if (lane == 0) {
+                    desc[q].t = g.nchunk == 1 ? item : item / g.nchunk;
+                    desc[q].c = chunk;
+                    desc[q].nsrc = nsrc;
+                }
+                for (int o = lane; o < nsrc; o += 32)
+                    desc[q].w[o] = l_w[bi * D + o];
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&qfull[q]);
+                const int col0 = chunk * g.CH;
+                const uint32_t bytes = (uint32_t)min(g.CH, g.H - col0) * 2u;
+                for (int o = lane; o < nsrc; o += 32) {
+                    const uint32_t u = use + o;
+                    const int b = (int)(u & (g.B - 1));
+                    if (u >= (uint32_t)g.B && !mbar_wait(&empty[b], ((u >> g.logB) - 1) & 1, kWaitNs)) {
+                        ok = false;
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&full[b], bytes);
+                    bulk_g2s(ring + (size_t)b * g.RB,
+                             y + ((int64_t)l_row[bi * D + o] * g.H + col0) * 2, bytes, &full[b]);
+                    last_use[b] = u;
+                }
+                use += nsrc;
+                if (!__all_sync(kFull, ok)) {
+                    bad |= EP_ERR_TIMEOUT;
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            __syncwarp();
+        }
+    } else {
+        // --------------------------------------------------------- consumers
+        const int ct = threadIdx.x - 32;
+        uint32_t use = 0, k = 0;
+        for (int item = blockIdx.x; item < n_items; item += stride, ++k) {
+            const int q = (int)(k % kQueue);
+            if (*abort_flag || !mbar_wait(&qfull[q], (k / kQueue) & 1, kWaitNs)) {
+                bad |= *abort_flag ? 0 : EP_ERR_TIMEOUT;
+                *abort_flag = 1;
+                break;
+            }
+            const int64_t t = desc[q].t;
+            const int col0 = desc[q].c * g.CH;
+            const int nsrc = desc[q].nsrc;
+            const int nv = min(g.CH, g.H - col0) / 8;
+            float acc[kVMax][8];
+#pragma unroll
+            for (int v = 0; v < kVMax; ++v)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[v][e] = 0.0f;
+            bool ok = true;
+            for (int o = 0; o < nsrc; ++o) {
+                const uint32_t u = use + o;
+                const int b = (int)(u & (g.B - 1));
+                if (!mbar_wait(&full[b], (u >> g.logB) & 1, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                const float wj = WEIGHTED ? desc[q].w[o] : 1.0f;
+                const uint4 *src = reinterpret_cast<const uint4 *>(ring + (size_t)b * g.RB);
+#pragma unroll
+                for (int v = 0; v < kVMax; ++v) {
+                    const int i = ct + v * kConsumers;
+                    if (i < nv) {
+                        const uint4 x = src[i];
+                        const float f[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
+                                            bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            acc[v][e] = WEIGHTED ? __fmaf_rn(wj, f[e], acc[v][e]) : __fadd_rn(acc[v][e], f[e]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[b]);
+            }
+            if (!ok) {
+                bad |= EP_ERR_TIMEOUT;
+                *abort_flag = 1;
+                break;
+            }
+            use += nsrc;
+#pragma unroll
+            for (int v = 0; v < kVMax; ++v) {
+                const int i = ct + v * kConsumers;
+                if (i >= nv)
+                    continue;
+                const int64_t e0 = t * g.H + col0 + (int64_t)i * 8;   // first element of this vector
+                if (OUT_F32) {
+                    float4 *o4 = reinterpret_cast<float4 *>(static_cast<float *>(out) + e0);
+                    o4[0] = make_float4(acc[v][0], acc[v][1], acc[v][2], acc[v][3]);
+                    o4[1] = make_float4(acc[v][4], acc[v][5], acc[v][6], acc[v][7]);
+                } else {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[v][0], acc[v][1]);
+                    o.y = pack_bf16x2(acc[v][2], acc[v][3]);
+                    o.z = pack_bf16x2(acc[v][4], acc[v][5]);
+                    o.w = pack_bf16x2(acc[v][6], acc[v][7]);
+                    st_stream(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + e0), o);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&qempty[q]);
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // copies this CTA armed may still be landing in its shared memory:
+        // wait for the last use of every buffer before the CTA exits
+        for (int b = 0; b < g.B; ++b)
+            if (last_use[b] >= 0)
+                (void)mbar_wait(&full[b], (uint32_t)(last_use[b] >> g.logB) & 1, kDrainNs);
+    }
+    raise(err, bad);
+}
+
+// ------------------------------------------------------------ launch policy --
+static int sm_count()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 148;
+    }
+    return n;
+}
+
+static GatherGeom gather_geometry(int H, int D)
+{
+    GatherGeom g;
+    g.H = H;
+    g.nchunk = (int)ceil_div(H, kMaxChunkCols);
+    g.CH = (int)align_up((size_t)ceil_div(H, g.nchunk), 8);
+    g.RB = (int)align_up((size_t)g.CH * 2, 128);
+    g.B = 1;
+    GatherGeom probe = g;
+    probe.B = 0;
+    const size_t fixed = gather_smem_bytes(probe, D);
+    const size_t fit = std::min<size_t>(kMaxBuffers, (kSmemBudget - fixed) / (g.RB + 2 * sizeof(uint64_t) + sizeof(int64_t)));
+    g.logB = 0;
+    while ((size_t)(2 << g.logB) <= fit)
+        ++g.logB;
+    g.B = 1 << g.logB;
+    return g;
+}
+
+template <class Rows, bool WEIGHTED, bool OUT_F32>
+static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, int64_t n_rows, int err_bits,
+                             void *out, int32_t *err, cudaStream_t stream)
+{
+    const int D = rows.len();
+    const GatherGeom g = gather_geometry(H, D);
+    const size_t smem = gather_smem_bytes(g, D);
+    auto kernel = gather_tma_kernel<Rows, WEIGHTED, OUT_F32>;
+    static size_t smem_set = 0;   // per instantiation; raising the limit is idempotent
+    if (smem > smem_set) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        smem_set = smem;
+    }
+    const int64_t items = T * g.nchunk;
+    if (items >= ((int64_t)1 << 31))
+        return EP_ERR_UNSUPPORTED;
+    const int grid = (int)std::min<int64_t>(items, sm_count());
+    if (grid == 0)
+        return EP_OK;
+    gather_tma_kernel<Rows, WEIGHTED, OUT_F32><<<grid, kGatherThreads, smem, stream>>>(
+        static_cast<const uint8_t *>(y), T, g, rows, n_rows, err_bits, out, err);
+    return launch_status();
+}
+
+static bool row_shape_ok(int64_t T, int H)
+{
+    return T >= 0 && H >= 8 && H % 8 == 0 && T < ((int64_t)1 << 31);
+}
+
+}  // namespace ep
+
+// ================================================================ C ABI ====
+using namespace ep;
+
+extern "C" int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
+                          int64_t num_send, void *out, int out_dtype, int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!row_shape_ok(T, H) || P < 1 || P > EP_MAX_RANKS || num_send < 0 || num_send >= ((int64_t)1 << 31))
+        return EP_ERR_INVALID_ARG;
+    if (out_dtype != 0 && out_dtype != 1)
+        return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (token_pos == nullptr || out == nullptr || !aligned(out, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (num_send > 0 && (y == nullptr || !aligned(y, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0)
+        return EP_OK;
+    const SendRows rows{token_pos, P};
+    if (out_dtype == 1)
+        return launch_gather_tma<SendRows, false, true>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err,
+                                                        stream);
+    return launch_gather_tma<SendRows, false, false>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err,
+                                                     stream);
+}
+
+extern "C" int ep_batched_combine(const void *y, const int64_t *topk_idx, const float *topk_weights,
+                                  const int32_t *slot, int64_t T, int K, int H, int E_local, int rank,
+                                  int max_num_tokens, void *out, int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || rank < 0 || max_num_tokens < 0)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * max_num_tokens >= ((int64_t)1 << 31))
+        return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (topk_idx == nullptr || topk_weights == nullptr || slot == nullptr || out == nullptr ||
+                  !aligned(out, 16)))
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * max_num_tokens > 0 && (y == nullptr || !aligned(y, 16)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0)
+        return EP_OK;
+    const BatchedRows rows{topk_idx, slot, topk_weights, K, (int64_t)rank * E_local, E_local, max_num_tokens, false};
+    return launch_gather_tma<BatchedRows, true, false>(y, T, H, rows, (int64_t)E_local * max_num_tokens,
+                                                       EP_ERR_CAPACITY, out, err, stream);
+}

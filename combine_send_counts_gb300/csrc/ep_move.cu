@@ -5,13 +5,9 @@
 //               expert-batched prepare (vLLM BatchedPrepareAndFinalize.prepare):
 //               every source row is read from HBM once and written to each of
 //               its destination rows.
-//   gather   -- combine (axolotl combine; Buffer.combine, addition without
-//               weights) and the batched combine (BatchedPrepareAndFinalize
-//               .finalize; Buffer.low_latency_combine, reduce with weights):
-//               every output row reads its source rows in a fixed order,
-//               accumulates in fp32 and is written once.
+//   (the combines live in ep_combine.cu)
 //
-// Both are HBM-bound copies.  A group of G threads (a multiple of 32) owns one
+// The scatter is an HBM-bound copy.  A group of G threads (a multiple of 32) owns one
 // token; each thread moves U 16-byte vectors of the row, so a row is covered
 // in one pass for H up to 8*G*U.  The destination (or source) row list of the
 // block's tokens is resolved once into shared memory.
@@ -22,54 +18,12 @@
 
 #include "ep_device.cuh"
 #include "ep_internal.h"
+#include "ep_rows.cuh"
 
 namespace ep {
 
 constexpr int kMoveThreads = 256;
-constexpr int kMaxList = 64;               // >= max(P, K)
 constexpr int kMaxTokensPerBlock = kMoveThreads / 32;
-
-// ------------------------------------------------------- row list sources --
-// Send layout: the rows of token t are token_pos[t, p] (p ascending), -1 = none.
-struct SendRows {
-    const int32_t *token_pos;
-    int P;
-    __device__ __forceinline__ int len() const { return P; }
-    __device__ __forceinline__ int32_t row(int64_t t, int j) const { return token_pos[t * P + j]; }
-    __device__ __forceinline__ float weight(int64_t, int) const { return 1.0f; }
-};
-
-// Expert-batched layout: slot k of token t names local expert e_l and slot s:
-// row e_l * M + s.  `dedup` drops a slot naming the same expert as an earlier
-// slot of the token (the scatter writes each (expert, token) row once; the
-// weighted combine keeps every slot's term).
-struct BatchedRows {
-    const int64_t *idx;
-    const int32_t *slot;
-    const float *w;
-    int K;
-    int64_t e0;
-    int E_local;
-    int M;
-    bool dedup;
-    __device__ __forceinline__ int len() const { return K; }
-    __device__ __forceinline__ int32_t row(int64_t t, int j) const
-    {
-        const int32_t s = slot[t * K + j];
-        const int64_t id = idx[t * K + j];
-        const int64_t el = id - e0;
-        if (s < 0 || el < 0 || el >= E_local)
-            return -1;
-        if (s >= M)                     // not a slot of this layout: reported by the caller
-            return INT32_MAX;
-        if (dedup)
-            for (int i = 0; i < j; ++i)
-                if (idx[t * K + i] == id)
-                    return -1;
-        return (int32_t)(el * M + s);
-    }
-    __device__ __forceinline__ float weight(int64_t t, int j) const { return w ? w[t * K + j] : 1.0f; }
-};
 
 struct Geometry {
     int nvec;   // 16-byte vectors per row (H / 8 for bf16)
@@ -218,75 +172,6 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
     }
 }
 
-// ---------------------------------------------------------- gather-reduce --
-// out[t] = sum_j w_j * y[row_j] over the token's list in order, fp32, from
-// +0.0f: a plain add when unweighted (send-layout combine), a fused
-// multiply-add when weighted (batched combine).
-template <int U, class Rows, bool WEIGHTED, bool OUT_F32>
-__global__ void __launch_bounds__(kMoveThreads)
-gather_kernel(const uint4 *__restrict__ y, int64_t T, Geometry g, Rows rows, int64_t n_rows,
-              int err_bits, void *__restrict__ out, int32_t *err)
-{
-    __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
-    __shared__ float s_w[WEIGHTED ? kMaxTokensPerBlock * kMaxList : 1];
-    const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
-    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, WEIGHTED ? s_w : nullptr, err);
-    __syncthreads();
-    const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
-    const int64_t t = t0 + s;
-    if (s >= g.tpb || t >= T)
-        return;
-    const int D = rows.len();
-    const int32_t *list = s_rows + s * kMaxList;
-    for (int base = 0; base < g.nvec; base += g.G * U) {
-        float acc[U][8];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[u][e] = 0.0f;
-        for (int j = 0; j < D; ++j) {
-            const int32_t r = list[j];
-            if (r < 0)
-                continue;
-            const float wj = WEIGHTED ? s_w[s * kMaxList + j] : 1.0f;
-            const uint4 *src = y + (int64_t)r * g.nvec;
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = base + lt + u * g.G;
-                v[u] = i < g.nvec ? ld_stream(src + i) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
-                                    bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    acc[u][e] = WEIGHTED ? __fmaf_rn(wj, f[e], acc[u][e]) : __fadd_rn(acc[u][e], f[e]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + lt + u * g.G;
-            if (i >= g.nvec)
-                continue;
-            if (OUT_F32) {
-                float4 *o = reinterpret_cast<float4 *>(out) + (t * g.nvec + i) * 2;
-                o[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-                o[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
-            } else {
-                uint4 o;
-                o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-                o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-                o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-                o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-                st_stream(reinterpret_cast<uint4 *>(out) + t * g.nvec + i, o);
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------- zero padding --
 // Zero rows [tokens_per_expert[e], M) of every local expert (16-byte stores).
 __global__ void zero_pad_kernel(uint4 *__restrict__ b_x, const int32_t *__restrict__ tokens_per_expert,
@@ -412,25 +297,6 @@ static int launch_scatter_fp8(const void *x, int64_t T, int H, const Rows &rows,
     return launch_status();
 }
 
-template <bool WEIGHTED, bool OUT_F32, class Rows>
-static int launch_gather(const void *y, int64_t T, int H, const Rows &rows, int64_t n_rows,
-                         int err_bits, void *out, int32_t *err, cudaStream_t stream)
-{
-    int U;
-    const Geometry g = geometry_for(H / 8, U);
-    const int64_t blocks = ceil_div(T, g.tpb);
-    if (blocks == 0)
-        return EP_OK;
-    auto *ys = static_cast<const uint4 *>(y);
-    switch (U) {
-    case 8: gather_kernel<8, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
-    case 4: gather_kernel<4, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
-    case 2: gather_kernel<2, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
-    default: gather_kernel<1, Rows, WEIGHTED, OUT_F32><<<blocks, g.G * g.tpb, 0, stream>>>(ys, T, g, rows, n_rows, err_bits, out, err); break;
-    }
-    return launch_status();
-}
-
 static bool row_shape_ok(int64_t T, int H)
 {
     return T >= 0 && H >= 8 && H % 8 == 0 && T < ((int64_t)1 << 31);
@@ -481,26 +347,6 @@ extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token
     return launch_scatter_bf16(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, err, stream);
 }
 
-extern "C" int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
-                          int64_t num_send, void *out, int out_dtype, int32_t *err, ep_stream_t stream_)
-{
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (!row_shape_ok(T, H) || P < 1 || P > EP_MAX_RANKS || num_send < 0 || num_send >= ((int64_t)1 << 31))
-        return EP_ERR_INVALID_ARG;
-    if (out_dtype != 0 && out_dtype != 1)
-        return EP_ERR_UNSUPPORTED;
-    if (T > 0 && (token_pos == nullptr || out == nullptr || !aligned(out, 16)))
-        return EP_ERR_INVALID_ARG;
-    if (num_send > 0 && (y == nullptr || !aligned(y, 16)))
-        return EP_ERR_INVALID_ARG;
-    if (T == 0)
-        return EP_OK;
-    const SendRows rows{token_pos, P};
-    if (out_dtype == 1)
-        return launch_gather<false, true>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err, stream);
-    return launch_gather<false, false>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err, stream);
-}
-
 extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
                                   int E_local, int rank, int max_num_tokens, void *b_x,
                                   int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws,
@@ -539,27 +385,6 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
         return launch_status();
     }
     return EP_OK;
-}
-
-extern "C" int ep_batched_combine(const void *y, const int64_t *topk_idx, const float *topk_weights,
-                                  const int32_t *slot, int64_t T, int K, int H, int E_local, int rank,
-                                  int max_num_tokens, void *out, int32_t *err, ep_stream_t stream_)
-{
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || rank < 0 || max_num_tokens < 0)
-        return EP_ERR_INVALID_ARG;
-    if ((int64_t)E_local * max_num_tokens >= ((int64_t)1 << 31))
-        return EP_ERR_UNSUPPORTED;
-    if (T > 0 && (topk_idx == nullptr || topk_weights == nullptr || slot == nullptr || out == nullptr ||
-                  !aligned(out, 16)))
-        return EP_ERR_INVALID_ARG;
-    if ((int64_t)E_local * max_num_tokens > 0 && (y == nullptr || !aligned(y, 16)))
-        return EP_ERR_INVALID_ARG;
-    if (T == 0)
-        return EP_OK;
-    const BatchedRows rows{topk_idx, slot, topk_weights, K, (int64_t)rank * E_local, E_local, max_num_tokens, false};
-    return launch_gather<true, false>(y, T, H, rows, (int64_t)E_local * max_num_tokens, EP_ERR_CAPACITY, out,
-                                      err, stream);
 }
 
 extern "C" int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,

@@ -100,25 +100,72 @@ count_kernel(const int64_t *__restrict__ idx, int K, int P, int E_local, ChunkTa
     raise(err, bad);
 }
 
+// Sum of `n` values strided by `stride`, with eight loads in flight at a time
+// (a plain loop would wait for each L2 round trip in turn).
+__device__ __forceinline__ int strided_sum(const int32_t *__restrict__ p, int n, int64_t stride)
+{
+    int s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int i = 0;
+    for (; i + 8 <= n; i += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            s[u] += p[(int64_t)(i + u) * stride];
+    }
+    for (; i < n; ++i)
+        s[0] += p[(int64_t)i * stride];
+    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
 // Single block: per-chunk send_counts and rank_offsets, tokens_per_expert.
+// Each column sum over the blocks' partials is split over `S` adjacent lanes
+// (S = 1024 / columns, a power of two up to 32) and joined with shuffles.
 __global__ void __launch_bounds__(1024)
 count_finish_kernel(const int32_t *__restrict__ part_rank, const int32_t *__restrict__ part_expert,
                     int nb, int P, int E, ChunkTable ct, int32_t *__restrict__ send_counts,
                     int32_t *__restrict__ rank_offsets, int32_t *__restrict__ tokens_per_expert)
 {
-    for (int i = threadIdx.x; i < ct.n * P; i += blockDim.x) {
-        const int c = i / P, p = i % P;
-        int s = 0;
-        for (int b = ct.first_block[c]; b < ct.first_block[c + 1]; ++b)
-            s += part_rank[(int64_t)b * P + p];
-        send_counts[i] = s;
+    __shared__ int32_t s_cnt[EP_MAX_CHUNKS * EP_MAX_RANKS];
+    const int CP = ct.n * P;
+    {
+        int S = 1;
+        while (S < 32 && CP * S * 2 <= (int)blockDim.x)
+            S *= 2;
+        for (int base = 0; base < CP * S; base += blockDim.x) {
+            const int i = base + threadIdx.x;
+            const int col = i / S, part = i % S;
+            int v = 0;
+            if (col < CP) {
+                const int c = col / P, p = col % P;
+                const int b0 = ct.first_block[c], nbc = ct.first_block[c + 1] - b0;
+                const int per = (nbc + S - 1) / S;
+                const int lo = min(nbc, part * per), hi = min(nbc, lo + per);
+                v = strided_sum(part_rank + (int64_t)(b0 + lo) * P + p, hi - lo, P);
+            }
+            for (int off = S / 2; off > 0; off >>= 1)
+                v += __shfl_down_sync(kFull, v, off, S);
+            if (col < CP && part == 0) {
+                send_counts[col] = v;
+                s_cnt[col] = v;
+            }
+        }
     }
     if (tokens_per_expert != nullptr) {
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            int s = 0;
-            for (int b = 0; b < nb; ++b)
-                s += part_expert[(int64_t)b * E + e];
-            tokens_per_expert[e] = s;
+        int S = 1;
+        while (S < 32 && E * S * 2 <= (int)blockDim.x)
+            S *= 2;
+        const int per = (nb + S - 1) / S;
+        for (int base = 0; base < E * S; base += blockDim.x) {
+            const int i = base + threadIdx.x;
+            const int e = i / S, part = i % S;
+            int v = 0;
+            if (e < E) {
+                const int lo = min(nb, part * per), hi = min(nb, lo + per);
+                v = strided_sum(part_expert + (int64_t)lo * E + e, hi - lo, E);
+            }
+            for (int off = S / 2; off > 0; off >>= 1)
+                v += __shfl_down_sync(kFull, v, off, S);
+            if (e < E && part == 0)
+                tokens_per_expert[e] = v;
         }
     }
     if (rank_offsets != nullptr) {
@@ -127,7 +174,7 @@ count_finish_kernel(const int32_t *__restrict__ part_rank, const int32_t *__rest
             int run = 0;
             for (int p = 0; p < P; ++p) {
                 rank_offsets[c * (P + 1) + p] = run;
-                run += send_counts[c * P + p];
+                run += s_cnt[c * P + p];
             }
             rank_offsets[c * (P + 1) + P] = run;
         }
@@ -203,25 +250,31 @@ layout_write_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // This block's first row per rank: all rows of earlier ranks, plus this
-    // rank's rows from earlier blocks.
+    // rank's rows from earlier blocks.  The partials are summed by every
+    // thread of the block (a few loads each) into shared counters.
+    __shared__ int32_t s_tot[EP_MAX_RANKS], s_before[EP_MAX_RANKS];
+    if (threadIdx.x < P) {
+        s_tot[threadIdx.x] = 0;
+        s_before[threadIdx.x] = 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb * P; i += blockDim.x) {
+        const int v = part_rank[i];
+        const int bb = i / P, p = i % P;
+        atomicAdd(&s_tot[p], v);
+        if (bb < b)
+            atomicAdd(&s_before[p], v);
+    }
+    __syncthreads();
     if (warp == 0) {
-        int tot[2] = {0, 0}, before[2] = {0, 0};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = lane + 32 * h;
-            if (p < P)
-                for (int bb = 0; bb < nb; ++bb) {
-                    const int v = part_rank[(int64_t)bb * P + p];
-                    tot[h] += v;
-                    before[h] += bb < b ? v : 0;
-                }
-        }
+        const int v0 = lane < P ? s_tot[lane] : 0;
+        const int v1 = lane + 32 < P ? s_tot[lane + 32] : 0;
         int e0, e1;
-        const int grand = warp_exclusive_scan64(tot[0], tot[1], e0, e1);
+        const int grand = warp_exclusive_scan64(v0, v1, e0, e1);
         if (lane < P)
-            s_base[lane] = e0 + before[0];
+            s_base[lane] = e0 + s_before[lane];
         if (lane + 32 < P)
-            s_base[lane + 32] = e1 + before[1];
+            s_base[lane + 32] = e1 + s_before[lane + 32];
         if (b == 0 && lane == 0 && (int64_t)grand != num_send)
             raise(err, EP_ERR_COUNT_MISMATCH);
     }
@@ -337,7 +390,7 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
                     const int32_t *__restrict__ part, int nb, int32_t *__restrict__ tokens_per_expert,
                     int32_t *__restrict__ slot, int32_t *err)
 {
-    __shared__ int32_t s_base[kGroup];
+    __shared__ int32_t s_base[kGroup], s_tot[kGroup];
     __shared__ int32_t s_warp[kWarps][kGroup];
     const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
     const bool valid = t < T;
@@ -350,19 +403,23 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
     for (int g0 = 0; g0 < E_local; g0 += kGroup) {
         const int ng = min(kGroup, E_local - g0);
         if (threadIdx.x < ng) {
-            const int e = g0 + threadIdx.x;
-            int tot = 0, before = 0;
-            for (int bb = 0; bb < nb; ++bb) {
-                const int v = part[(int64_t)bb * E_local + e];
-                tot += v;
-                before += bb < (int)blockIdx.x ? v : 0;
-            }
-            s_base[threadIdx.x] = before;
-            if (blockIdx.x == 0) {
-                tokens_per_expert[e] = min(tot, M);
-                if (tot > M)
-                    bad = EP_ERR_CAPACITY;
-            }
+            s_base[threadIdx.x] = 0;
+            s_tot[threadIdx.x] = 0;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nb * ng; i += blockDim.x) {
+            const int bb = i / ng, e = i % ng;
+            const int v = part[(int64_t)bb * E_local + g0 + e];
+            atomicAdd(&s_tot[e], v);
+            if (bb < (int)blockIdx.x)
+                atomicAdd(&s_base[e], v);
+        }
+        __syncthreads();
+        if (blockIdx.x == 0 && threadIdx.x < ng) {
+            const int tot = s_tot[threadIdx.x];
+            tokens_per_expert[g0 + threadIdx.x] = min(tot, M);
+            if (tot > M)
+                bad = EP_ERR_CAPACITY;
         }
         const uint64_t mask = valid ? local_mask(idx + t * K, K, e0 + g0, ng) : 0;
         for (int e = 0; e < ng; ++e) {

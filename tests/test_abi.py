@@ -65,3 +65,25 @@ def test_argument_checks_reject_before_launch(lib):
                                ctypes.c_int, vp, vp]
     assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 2, None, None) == ep.EP_ERR_UNSUPPORTED  # out_dtype
     assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # null out
+
+
+def test_no_entry_point_host_code_calls_exit(lib):
+    # nvcc compiles a host-side call of a __device__-only function inside a
+    # template into exit(1) without a diagnostic; an entry point built that
+    # way ends the caller's process silently.  Inspect the host code of this
+    # (locally built) library for direct calls of exit.
+    import shutil
+    import subprocess
+    objdump = shutil.which("objdump")
+    if objdump is None:
+        pytest.skip("objdump not available")
+    asm = subprocess.run([objdump, "-d", "--no-show-raw-insn", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    fn, offenders = None, set()
+    for line in asm.splitlines():
+        m = re.match(r"^[0-9a-f]+ <(.+)>:$", line)
+        if m:
+            fn = m.group(1)
+        elif re.search(r"\s(call|bl|jmp|b)\s+[0-9a-f]+ <exit@plt>", line):
+            offenders.add(fn)
+    assert not offenders, offenders
