@@ -1,12 +1,14 @@
 """Benchmark: MoE top-k dispatch + combine on one GB300 (or N replicas).
 
-One step is the whole hot path on one batch of synthetic input, as the axolotl
-``integrations.expert_parallel.torch_dispatch`` page lays it out for the
-collective-free local path:
-
-    compute_send_counts -> one device->host copy of the counts ->
-    build_send_layout(num_send from the host) -> dispatch (row scatter) ->
-    combine (per-token sum of the expert outputs)
+One step is the whole hot path on one batch of synthetic input: the routing
+metadata (compute_send_counts + build_send_layout of the axolotl
+``integrations.expert_parallel.torch_dispatch`` page), dispatch (row scatter)
+and combine (per-token sum of the expert outputs).  The timed step uses the
+no-host-sync form (worst-case row buffers, the "num_worst_tokens" mode of the
+NeMo ``uccl_ep.buffer`` page); the pages' host-synchronising call order
+(counts -> device->host copy -> layout(num_send)) is timed too and reported
+under ``host_sync_path``, and a CUDA-graph replay of the step under
+``graph_replay``.
 
 on the large skewed workload (T=16384, H=7168 bf16, E=256, K=8, P=8 logical
 ranks, Zipf(1.2) routing).  Inputs are resident in HBM when a step starts; L2
@@ -154,11 +156,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ GPU arm --
 class SendPath:
-    """All device buffers of the send-layout path, allocated once."""
+    """All device buffers of the send-layout path, allocated once.
+
+    Two ways through the same kernels:
+      nosync -- ep_route_nosync (counts + layout, rows sized for the worst
+                case T*min(K,P), no host round trip) -> ep_dispatch ->
+                ep_combine; 4 launches, nothing waits on the host;
+      sync   -- ep_compute_send_counts -> device-to-host copy of the counts and
+                a host wait -> ep_build_send_layout(num_send) -> ep_dispatch ->
+                ep_combine; 6 launches.
+    """
 
     def __init__(self, ep, torch, w, x, idx, wts, dev):
         self.ep, self.torch, self.w = ep, torch, w
-        T, K, P, El, H = w.T, w.K, w.P, w.E_local, w.H
+        T, K, P, El = w.T, w.K, w.P, w.E_local
         self.x, self.idx, self.wts = x, idx, wts
         i32, u8 = torch.int32, torch.uint8
         self.dest = torch.empty((T, K), dtype=i32, device=dev)
@@ -174,15 +185,35 @@ class SendPath:
     def alloc_rows(self, N):
         torch, w, dev = self.torch, self.w, self.x.device
         self.N = N
-        self.send_token_idx = torch.empty(N, dtype=torch.int32, device=dev)
-        self.send_rank = torch.empty(N, dtype=torch.int32, device=dev)
-        self.send_idx = torch.empty((N, w.K), dtype=torch.int64, device=dev)
-        self.send_w = torch.empty((N, w.K), dtype=torch.float32, device=dev)
-        self.recv_x = torch.empty((N, w.H), dtype=torch.bfloat16, device=dev)
+        self.W = w.T * min(w.K, w.P)          # worst-case rows of the no-sync path
+        W = self.W
+        self.send_token_idx = torch.empty(W, dtype=torch.int32, device=dev)
+        self.send_rank = torch.empty(W, dtype=torch.int32, device=dev)
+        self.send_idx = torch.empty((W, w.K), dtype=torch.int64, device=dev)
+        self.send_w = torch.empty((W, w.K), dtype=torch.float32, device=dev)
+        self.recv_x = torch.empty((W, w.H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
 
-    def step(self, y, stream, ev=None):
-        """One pass of the hot path; ev = list of 5 events (or None)."""
+    def step_nosync(self, y, stream, ev=None):
+        """ev: 4 events (start, after route, after dispatch, after combine) or None."""
+        ep, w = self.ep, self.w
+        T, K, P, El, H, W = w.T, w.K, w.P, w.E_local, w.H, self.W
+        if ev is not None:
+            ev[0].record(stream)
+        ep.ep_route_nosync(self.idx, self.wts, T, K, P, El, W, self.dest, self.is_in_rank, self.send_counts,
+                           self.rank_offsets, None, self.send_token_idx, self.send_rank, self.send_idx, self.send_w,
+                           self.token_pos, self.ws, self.err, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ep.ep_dispatch(self.x, T, H, self.token_pos, P, W, self.recv_x, None, 0, self.err, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        ep.ep_combine(y, T, H, self.token_pos, P, W, self.out, 0, self.err, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    def step_sync(self, y, stream, ev=None):
+        """ev: 6 events (start, counts, host sync, layout, dispatch, combine) or None."""
         ep, w = self.ep, self.w
         T, K, P, El, H = w.T, w.K, w.P, w.E_local, w.H
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
@@ -206,7 +237,27 @@ class SendPath:
         rec(5)
 
 
-LAUNCHES_PER_STEP = 6   # counts: 2, layout: 2, dispatch: 1, combine: 1
+LAUNCHES_PER_STEP = 4   # route: 2 (counts, layout), dispatch: 1, combine: 1
+
+
+def _timed_steps(torch, steps, flush, step, n_events):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()          # outside the events; the step is enqueued while it runs
+        step(evs[k])
+    torch.cuda.synchronize()
+    return evs
+
+
+def _kernel_table(ab, parts):
+    kern = {}
+    for name, times in parts.items():
+        us = statistics.mean(times) * 1e3
+        kern[name] = {"us": round(us, 2)}
+        if name in ab:
+            kern[name]["algorithmic_bytes"] = ab[name]
+            kern[name]["gbs"] = round(ab[name] / (us * 1e-6) / 1e9, 1)
+    return kern
 
 
 def run_gpu(args):
@@ -238,52 +289,88 @@ def run_gpu(args):
     N = int(sp.send_counts.sum().item())
     sp.alloc_rows(N)
     y_h = wl.expert_outputs(w, N)
-    y = y_h.to(dev)
+    y = torch.empty((sp.W, w.H), dtype=torch.bfloat16, device=dev)   # expert outputs in worst-case rows
+    y[:N].copy_(y_h)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     for _ in range(max(args.warmup, 0)):
         flush.zero_()
-        sp.step(y, stream)
+        sp.step_nosync(y, stream)
+        flush.zero_()
+        sp.step_sync(y, stream)
     torch.cuda.synchronize()
     if int(sp.err.item()) != 0:
         raise ep.EPError(int(sp.err.item()), "warmup")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # ---- timed region: the no-sync path
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
-        for k in range(args.steps):
-            flush.zero_()
-            sp.step(y, stream, evs[k])
-        torch.cuda.synchronize()
+        evs = _timed_steps(torch, args.steps, flush, lambda e: sp.step_nosync(y, stream, e), 4)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     if int(sp.err.item()) != 0:
         raise ep.EPError(int(sp.err.item()), "timed steps")
-
-    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
-    parts = {"counts": [e[0].elapsed_time(e[1]) for e in evs],
-             "counts_d2h_sync": [e[1].elapsed_time(e[2]) for e in evs],
-             "layout": [e[2].elapsed_time(e[3]) for e in evs],
-             "dispatch": [e[3].elapsed_time(e[4]) for e in evs],
-             "combine": [e[4].elapsed_time(e[5]) for e in evs]}
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    parts = {"route": [e[0].elapsed_time(e[1]) for e in evs],
+             "dispatch": [e[1].elapsed_time(e[2]) for e in evs],
+             "combine": [e[2].elapsed_time(e[3]) for e in evs]}
     total_s = sum(step_ms) / 1e3
     tok_s, max_s = aggregate(total_s, float(w.T * args.steps), world, dist if world > 1 else None)
 
     peak, peak_src = measured_peak()
     ab = algorithmic_bytes(w.T, w.H, N, w.K, w.P)
-    kern = {}
-    for name in ("counts", "layout", "dispatch", "combine"):
-        us = statistics.mean(parts[name]) * 1e3
-        kern[name] = {"us": round(us, 2), "algorithmic_bytes": ab[name],
-                      "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1)}
-    kern["counts_d2h_sync"] = {"us": round(statistics.mean(parts["counts_d2h_sync"]) * 1e3, 2)}
+    ab["route"] = ab.pop("counts") + ab.pop("layout")
+    kern = _kernel_table(ab, parts)
     dom = max(("dispatch", "combine"), key=lambda k: kern[k]["us"])
     step_bytes = sum(ab.values())
-    mean_step_ms = statistics.mean(step_ms)
-    achieved_step = step_bytes / (mean_step_ms * 1e-3) / 1e9
+    achieved_step = step_bytes / (statistics.mean(step_ms) * 1e-3) / 1e9
+
+    # ---- the same step through the host-synchronising calls (pages' call order)
+    evs_s = _timed_steps(torch, args.steps, flush, lambda e: sp.step_sync(y, stream, e), 6)
+    ms_s = [e[0].elapsed_time(e[5]) for e in evs_s]
+    ab_s = algorithmic_bytes(w.T, w.H, N, w.K, w.P)
+    sync_path = {
+        "value": round(w.T * len(ms_s) / (sum(ms_s) / 1e3), 1), "unit": "tokens/s",
+        "ms_per_step": round(statistics.mean(ms_s), 4),
+        "path": "ep_compute_send_counts -> D2H counts + host wait -> ep_build_send_layout(num_send) -> "
+                "ep_dispatch -> ep_combine",
+        "kernels": _kernel_table(ab_s, {
+            "counts": [e[0].elapsed_time(e[1]) for e in evs_s],
+            "counts_d2h_host_wait": [e[1].elapsed_time(e[2]) for e in evs_s],
+            "layout": [e[2].elapsed_time(e[3]) for e in evs_s],
+            "dispatch": [e[3].elapsed_time(e[4]) for e in evs_s],
+            "combine": [e[4].elapsed_time(e[5]) for e in evs_s]}),
+    }
+
+    # ---- the no-sync step replayed from a CUDA graph
+    graph_path = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            sp.step_nosync(y, side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            sp.step_nosync(y, side)
+        torch.cuda.synchronize()
+        gt = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            g.replay()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            gt.append(a0.elapsed_time(a1))
+        graph_path = {"value": round(w.T * len(gt) / (sum(gt) / 1e3), 1), "unit": "tokens/s",
+                      "ms_per_step": round(statistics.mean(gt), 4),
+                      "hbm_gbs": round(step_bytes / (statistics.mean(gt) * 1e-3) / 1e9, 1)}
+        if int(sp.err.item()) != 0:
+            raise ep.EPError(int(sp.err.item()), "graph replay")
 
     result = {
         "metric": METRIC,
@@ -300,10 +387,12 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {"workload": f"{w.name}: T={w.T} H={w.H} E={w.E} K={w.K} P={w.P} E_local={w.E_local} "
                                f"routing={w.routing}({w.zipf_s}) weights={w.weights}",
-                   "N_rows": N, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "N_rows": N, "worst_case_rows": sp.W,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write, outside the timed events); "
                          "working set 1.8 GB > L2",
-                   "path": "counts -> D2H counts + host sync -> layout -> dispatch -> combine",
+                   "path": "ep_route_nosync (counts + layout, worst-case rows, no host round trip) -> "
+                           "ep_dispatch -> ep_combine",
                    "seed": w.seed},
         "hbm_gbs": round(achieved_step, 1),
         "hbm_frac_of_peak": round(achieved_step / peak, 4),
@@ -314,10 +403,12 @@ def run_gpu(args):
         "kernels": kern,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
+        "host_sync_path": sync_path,
+        "graph_replay": graph_path,
     }
 
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, stream, world, dist)
+        result["e2e"] = run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, y, stream, world, dist)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, x_h, idx_h, w_h, y_h, args.cpu_steps, full=True)
     if world > 1:
@@ -327,15 +418,15 @@ def run_gpu(args):
         print(json.dumps(result), flush=True)
 
 
-def run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, stream, world, dist):
-    """Same step through the C ABI from pinned HOST buffers: H2D of the inputs
-    and the expert outputs, the path, D2H of the combined result, all inside
-    the timed events."""
+def run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, y_dev, stream, world, dist):
+    """The same no-sync step through the C ABI from pinned HOST buffers: H2D of
+    the inputs and of the expert outputs, the path, D2H of the combined
+    result, all inside the timed events."""
     xp, ip, wp, yp = (t.pin_memory() for t in (x_h, idx_h, w_h, y_h))
     outp = torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True)
-    y_d = torch.empty_like(yp, device=sp.x.device)
+    N = y_h.shape[0]
     h2d = sum(t.numel() * t.element_size() for t in (xp, ip, wp, yp))
-    d2h = outp.numel() * outp.element_size() + w.P * 4
+    d2h = outp.numel() * outp.element_size()
     times = []
     for k in range(args.e2e_warmup + args.e2e_steps):
         a = torch.cuda.Event(enable_timing=True)
@@ -344,8 +435,8 @@ def run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, stream, world, dist):
         sp.x.copy_(xp, non_blocking=True)
         sp.idx.copy_(ip, non_blocking=True)
         sp.wts.copy_(wp, non_blocking=True)
-        y_d.copy_(yp, non_blocking=True)
-        sp.step(y_d, stream)
+        y_dev[:N].copy_(yp, non_blocking=True)
+        sp.step_nosync(y_dev, stream)
         outp.copy_(sp.out, non_blocking=True)
         b.record(stream)
         b.synchronize()
@@ -422,6 +513,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-warmup", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")

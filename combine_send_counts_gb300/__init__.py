@@ -66,6 +66,8 @@ _SIGNATURES = {
                                   _VP, _SZ, _VP, _VP]),
     "ep_batched_combine": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
     "ep_local_expert_fp8": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP]),
+    "ep_route_nosync": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                               _VP, _VP, _VP, _SZ, _VP, _VP]),
     "ep_compute_send_counts_noalloc": (_I32, [_VP, _I64, _I32, _I32, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
                                               _VP, _VP]),
 }
@@ -149,6 +151,16 @@ def ep_build_send_layout(topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_lo
                                      _p(send_idx), _p(send_w), _p(token_pos), _p(ws),
                                      ws.numel() * ws.element_size(), _p(err), _stream(stream))
     _check(rc, "ep_build_send_layout")
+
+
+def ep_route_nosync(topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
+                    rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos, ws, err,
+                    stream=None):
+    rc = load().ep_route_nosync(_p(topk_idx), _p(topk_weights), int(T), int(K), int(P), int(E_local),
+                                int(num_worst_rows), _p(dest), _p(is_in_rank), _p(send_counts), _p(rank_offsets),
+                                _p(tokens_per_expert), _p(send_token_idx), _p(send_rank), _p(send_idx), _p(send_w),
+                                _p(token_pos), _p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream))
+    _check(rc, "ep_route_nosync")
 
 
 def ep_dispatch(x, T, H, token_pos, P, num_send, recv_x, recv_scale, fp8, err, stream=None):
@@ -265,6 +277,36 @@ def build_send_layout(topk_idx, topk_weights, dest, is_in_rank, num_send: int, n
     ep_build_send_layout(topk_idx, topk_weights, dest, is_in_rank, T, K, P, num_local_experts, N,
                          out["send_token_idx"], out["send_rank"], out["send_idx"], out["send_w"],
                          out["token_pos"], ws, err, stream)
+    out["err"] = err
+    return out
+
+
+def route_nosync(topk_idx, topk_weights, num_ranks: int, num_local_experts: int, num_worst_rows: Optional[int] = None,
+                 ws=None, err=None, stream=None, with_tokens_per_expert: bool = True):
+    """Counts and send layout in one call with rows sized for the worst case
+    (no host round trip).  rank_offsets[P] holds the number of rows used."""
+    T, K = topk_idx.shape
+    P, El = num_ranks, num_local_experts
+    W = T * min(K, P) if num_worst_rows is None else int(num_worst_rows)
+    dev = topk_idx.device
+    out = dict(
+        dest=torch.empty((T, K), dtype=torch.int32, device=dev),
+        is_in_rank=torch.empty((T, P), dtype=torch.uint8, device=dev),
+        send_counts=torch.empty(P, dtype=torch.int32, device=dev),
+        rank_offsets=torch.empty(P + 1, dtype=torch.int32, device=dev),
+        tokens_per_expert=torch.empty(P * El, dtype=torch.int32, device=dev) if with_tokens_per_expert else None,
+        send_token_idx=torch.empty(W, dtype=torch.int32, device=dev),
+        send_rank=torch.empty(W, dtype=torch.int32, device=dev),
+        send_idx=torch.empty((W, K), dtype=torch.int64, device=dev),
+        send_w=torch.empty((W, K), dtype=torch.float32, device=dev),
+        token_pos=torch.empty((T, P), dtype=torch.int32, device=dev),
+        num_worst_rows=W,
+    )
+    ws = ws if ws is not None else workspace(T, K, P, El, 1, dev)
+    err = err if err is not None else error_word(dev)
+    ep_route_nosync(topk_idx, topk_weights, T, K, P, El, W, out["dest"], out["is_in_rank"], out["send_counts"],
+                    out["rank_offsets"], out["tokens_per_expert"], out["send_token_idx"], out["send_rank"],
+                    out["send_idx"], out["send_w"], out["token_pos"], ws, err, stream)
     out["err"] = err
     return out
 

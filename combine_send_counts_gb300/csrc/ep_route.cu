@@ -235,31 +235,66 @@ __device__ __forceinline__ int warp_exclusive_scan64(int v0, int v1, int &e0, in
     return s0 + s1;
 }
 
-__global__ void __launch_bounds__(kRouteThreads)
-layout_write_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w,
-                    const int32_t *__restrict__ dest, const uint8_t *__restrict__ is_in_rank,
-                    int64_t T, int K, int P, int E_local, int64_t num_send,
-                    const int32_t *__restrict__ part_rank, int nb,
-                    int32_t *__restrict__ send_token_idx, int32_t *__restrict__ send_rank,
-                    int64_t *__restrict__ send_idx, float *__restrict__ send_w,
-                    int32_t *__restrict__ token_pos, int32_t *err)
+// Lane of the r-th (0-based) set bit of m; r < popc(m).  Binary search over
+// halves, so the result is always a lane in [0, 32).
+__device__ __forceinline__ int nth_set_bit(unsigned m, int r)
+{
+    int pos = 0;
+#pragma unroll
+    for (int width = 16; width > 0; width >>= 1) {
+        const int c = __popc(m & ((1u << width) - 1u));
+        if (r >= c) {
+            r -= c;
+            m >>= width;
+            pos += width;
+        }
+    }
+    return pos;
+}
+
+// Outputs and mode of layout_write_kernel.
+struct LayoutArgs {
+    const int64_t *idx;
+    const float *w;
+    const int32_t *dest;
+    const uint8_t *is_in_rank;
+    int64_t T;
+    int K, P, E_local;
+    int64_t num_rows;         // rows in the caller's send buffers
+    int exact;                // 1: the routed count must equal num_rows; 0: num_rows is a worst-case capacity
+    const int32_t *part_rank; // [nb][P] block partials
+    int nb;
+    const int32_t *part_expert;   // [nb][E] or null
+    int32_t *send_counts;     // [P] or null (written by block 0)
+    int32_t *rank_offsets;    // [P+1] or null (written by block 0)
+    int32_t *tokens_per_expert;   // [E] or null (experts split over the blocks)
+    int32_t *send_token_idx, *send_rank;
+    int64_t *send_idx;
+    float *send_w;
+    int32_t *token_pos;
+    int32_t *err;
+};
+
+// One block of 256 tokens: the block's first row per rank from the partials,
+// each lane's row from warp ballots, then the rows.  A warp writes the K-wide
+// send_idx / send_w rows of its tokens for one rank together: its rows for
+// rank p are consecutive, so the warp covers them with consecutive stores.
+__global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs a)
 {
     __shared__ int32_t s_base[EP_MAX_RANKS];
+    __shared__ int32_t s_tot[EP_MAX_RANKS], s_before[EP_MAX_RANKS];
     __shared__ int32_t s_warp[kWarps][EP_MAX_RANKS];
+    const int P = a.P, K = a.K;
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // This block's first row per rank: all rows of earlier ranks, plus this
-    // rank's rows from earlier blocks.  The partials are summed by every
-    // thread of the block (a few loads each) into shared counters.
-    __shared__ int32_t s_tot[EP_MAX_RANKS], s_before[EP_MAX_RANKS];
     if (threadIdx.x < P) {
         s_tot[threadIdx.x] = 0;
         s_before[threadIdx.x] = 0;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < nb * P; i += blockDim.x) {
-        const int v = part_rank[i];
+    for (int i = threadIdx.x; i < a.nb * P; i += blockDim.x) {
+        const int v = a.part_rank[i];
         const int bb = i / P, p = i % P;
         atomicAdd(&s_tot[p], v);
         if (bb < b)
@@ -275,13 +310,55 @@ layout_write_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w
             s_base[lane] = e0 + s_before[lane];
         if (lane + 32 < P)
             s_base[lane + 32] = e1 + s_before[lane + 32];
-        if (b == 0 && lane == 0 && (int64_t)grand != num_send)
-            raise(err, EP_ERR_COUNT_MISMATCH);
+        if (b == 0) {
+            if (a.send_counts != nullptr) {
+                if (lane < P)
+                    a.send_counts[lane] = v0;
+                if (lane + 32 < P)
+                    a.send_counts[lane + 32] = v1;
+            }
+            if (a.rank_offsets != nullptr) {
+                if (lane < P)
+                    a.rank_offsets[lane] = e0;
+                if (lane + 32 < P)
+                    a.rank_offsets[lane + 32] = e1;
+                if (lane == 0)
+                    a.rank_offsets[P] = grand;
+            }
+            if (lane == 0) {
+                if (a.exact && (int64_t)grand != a.num_rows)
+                    raise(a.err, EP_ERR_COUNT_MISMATCH);
+                if (!a.exact && (int64_t)grand > a.num_rows)
+                    raise(a.err, EP_ERR_CAPACITY);
+            }
+        }
+    }
+    if (a.tokens_per_expert != nullptr) {
+        // experts b, b + nb, ...: every thread adds one block partial at a time
+        const int E = P * a.E_local;
+        const int mine = (E - b + a.nb - 1) / a.nb;
+        int32_t *s_tpe = &s_warp[0][0];   // reused before the ballots below
+        constexpr int kRound = kWarps * EP_MAX_RANKS;
+        for (int j0 = 0; j0 < mine; j0 += kRound) {
+            const int m = min(kRound, mine - j0);
+            for (int j = threadIdx.x; j < m; j += blockDim.x)
+                s_tpe[j] = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < m * a.nb; i += blockDim.x) {
+                const int j = i / a.nb, bb = i % a.nb;
+                atomicAdd(&s_tpe[j], a.part_expert[(int64_t)bb * E + b + (j0 + j) * a.nb]);
+            }
+            __syncthreads();
+            for (int j = threadIdx.x; j < m; j += blockDim.x)
+                a.tokens_per_expert[b + (j0 + j) * a.nb] = s_tpe[j];
+            __syncthreads();
+        }
     }
 
-    const int64_t t = (int64_t)b * kRouteThreads + threadIdx.x;
-    const bool valid = t < T;
-    const uint64_t mask = valid ? rank_mask(is_in_rank, t, P) : 0;
+    const int64_t t0 = (int64_t)b * kRouteThreads + warp * 32;   // first token of this warp
+    const int64_t t = t0 + lane;
+    const bool valid = t < a.T;
+    const uint64_t mask = valid ? rank_mask(a.is_in_rank, t, P) : 0;
     for (int p = 0; p < P; ++p) {
         const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
         if (lane == 0)
@@ -302,7 +379,7 @@ layout_write_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w
     if (valid) {
         uint64_t dmask = 0;
         for (int k = 0; k < K; ++k) {
-            const int d = dest[t * K + k];
+            const int d = a.dest[t * K + k];
             if (d >= 0 && d < P)
                 dmask |= 1ull << d;
         }
@@ -311,27 +388,41 @@ layout_write_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w
     }
     for (int p = 0; p < P; ++p) {
         const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
-        if (!valid)
+        if (bal == 0) {
+            if (valid)
+                a.token_pos[t * P + p] = -1;
             continue;
-        int32_t n = -1;
-        if ((mask >> p) & 1ull) {
-            const int64_t pos = (int64_t)s_base[p] + s_warp[warp][p] + __popc(bal & lanemask_lt());
-            if (pos < num_send) {
-                n = (int32_t)pos;
-                send_token_idx[n] = (int32_t)t;
-                send_rank[n] = p;
-                for (int k = 0; k < K; ++k) {
-                    const bool own = dest[t * K + k] == p;
-                    send_idx[(int64_t)n * K + k] = own ? idx[t * K + k] - (int64_t)p * E_local : -1;
-                    send_w[(int64_t)n * K + k] = own ? w[t * K + k] : 0.0f;
-                }
-            } else {
-                bad = EP_ERR_COUNT_MISMATCH;
-            }
         }
-        token_pos[t * P + p] = n;
+        const int64_t n0 = (int64_t)s_base[p] + s_warp[warp][p];   // this warp's first row for rank p
+        if (valid) {
+            int32_t n = -1;
+            if ((mask >> p) & 1ull) {
+                const int64_t pos = n0 + __popc(bal & lanemask_lt());
+                if (pos < a.num_rows) {
+                    n = (int32_t)pos;
+                    a.send_token_idx[n] = (int32_t)t;
+                    a.send_rank[n] = p;
+                } else {
+                    bad = a.exact ? EP_ERR_COUNT_MISMATCH : EP_ERR_CAPACITY;
+                }
+            }
+            a.token_pos[t * P + p] = n;
+        }
+        // K-wide rows n0 .. n0 + cnt - 1, written by the warp together
+        const int cnt = __popc(bal);
+        for (int e = lane; e < cnt * K; e += 32) {
+            const int r = e / K, k = e - r * K;
+            const int64_t n = n0 + r;
+            if (n >= a.num_rows)
+                break;
+            const int src = nth_set_bit(bal, r);
+            const int64_t ts = t0 + src;
+            const bool own = a.dest[ts * K + k] == p;
+            a.send_idx[n * K + k] = own ? a.idx[ts * K + k] - (int64_t)p * a.E_local : -1;
+            a.send_w[n * K + k] = own ? a.w[ts * K + k] : 0.0f;
+        }
     }
-    raise(err, bad);
+    raise(a.err, bad);
 }
 
 // ---------------------------------------------------- expert-batched slots --
@@ -592,9 +683,59 @@ extern "C" int ep_build_send_layout(const int64_t *topk_idx, const float *topk_w
     layout_count_kernel<<<nb, kRouteThreads, 0, stream>>>(is_in_rank, T, P, part_rank);
     if (launch_status() != EP_OK)
         return EP_ERR_CUDA;
-    layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, topk_weights, dest, is_in_rank, T, K, P,
-                                                          E_local, num_send, part_rank, nb, send_token_idx,
-                                                          send_rank, send_idx, send_w, token_pos, err);
+    LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_send, 1, part_rank, nb,
+                 nullptr, nullptr, nullptr, nullptr, send_token_idx, send_rank, send_idx, send_w, token_pos, err};
+    layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);
+    return launch_status();
+}
+
+extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
+                               int E_local, int64_t num_worst_rows, int32_t *dest, uint8_t *is_in_rank,
+                               int32_t *send_counts, int32_t *rank_offsets, int32_t *tokens_per_expert,
+                               int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w,
+                               int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!routing_shape_ok(T, K, P, E_local) || num_worst_rows < 0 || num_worst_rows >= ((int64_t)1 << 31))
+        return EP_ERR_INVALID_ARG;
+    if (ws == nullptr || !aligned(ws, kWsAlign) || ws_bytes < ep_workspace_size(T, K, P, E_local, 1))
+        return EP_ERR_INVALID_ARG;
+    if (send_counts == nullptr || rank_offsets == nullptr)
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (topk_idx == nullptr || topk_weights == nullptr || dest == nullptr || is_in_rank == nullptr ||
+                  token_pos == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (num_worst_rows > 0 && (send_token_idx == nullptr || send_rank == nullptr || send_idx == nullptr ||
+                               send_w == nullptr))
+        return EP_ERR_INVALID_ARG;
+    const int nb = (int)ceil_div(T, kRouteThreads);
+    const int E = P * E_local;
+    int32_t *part_rank = static_cast<int32_t *>(ws);
+    int32_t *part_expert = reinterpret_cast<int32_t *>(
+        static_cast<char *>(ws) + align_up((size_t)route_blocks_max(T, 1) * P * sizeof(int32_t), kWsAlign));
+    if (nb == 0) {   // nothing routed: zero counts through the single-chunk finish
+        ChunkTable ct{};
+        ct.n = 1;
+        count_finish_kernel<<<1, 1024, 0, stream>>>(part_rank, nullptr, 0, P, E, ct, send_counts, rank_offsets,
+                                                    tokens_per_expert);
+        return launch_status();
+    }
+    ChunkTable ct{};
+    ct.n = 1;
+    ct.start[0] = 0;
+    ct.start[1] = T;
+    ct.first_block[0] = 0;
+    ct.first_block[1] = nb;
+    int32_t *pe = tokens_per_expert != nullptr ? part_expert : nullptr;
+    const size_t smem = sizeof(int32_t) * (kWarps * P + (pe != nullptr ? E : 0));
+    count_kernel<<<nb, kRouteThreads, smem, stream>>>(topk_idx, K, P, E_local, ct, dest, is_in_rank, part_rank, pe,
+                                                      err);
+    if (launch_status() != EP_OK)
+        return EP_ERR_CUDA;
+    LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_worst_rows, 0, part_rank, nb,
+                 pe, send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
+                 token_pos, err};
+    layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);
     return launch_status();
 }
 

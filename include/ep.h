@@ -113,7 +113,8 @@ int ep_compute_send_counts(const int64_t *topk_idx, int64_t T, int K, int P, int
  *     send_token_idx [N], send_rank [N], send_idx [N,K] int64, send_w [N,K]
  *     fp32.  It must equal sum(is_in_rank) (passing it from the host avoids
  *     a device sync, [AX] build_send_layout); a different device count sets
- *     EP_ERR_COUNT_MISMATCH and rows at or past num_send are not written.
+ *     EP_ERR_COUNT_MISMATCH and rows at or past num_send are not written
+ *     (with T == 0 a non-zero num_send is returned as EP_ERR_COUNT_MISMATCH).
  * Device errors: EP_ERR_COUNT_MISMATCH. */
 int ep_build_send_layout(const int64_t *topk_idx, const float *topk_weights,
                          const int32_t *dest, const uint8_t *is_in_rank,
@@ -121,6 +122,28 @@ int ep_build_send_layout(const int64_t *topk_idx, const float *topk_weights,
                          int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx,
                          float *send_w, int32_t *token_pos,
                          void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
+/* [AX] compute_send_counts followed by build_send_layout, without the host
+ * round trip: the [UB] Buffer.dispatch "num_worst_tokens" mode, where the
+ * receive buffers are sized for the worst case so that no CPU sync is needed
+ * and the call can be enqueued back to back (or captured in a CUDA graph).
+ * Computes the outputs of both calls for one chunk:
+ *   dest, is_in_rank, send_counts [P], rank_offsets [P+1] (rank_offsets[P] =
+ *   N, the number of rows the layout uses), tokens_per_expert [P*E_local] or
+ *   NULL, and the send layout rows send_token_idx, send_rank, send_idx,
+ *   send_w and token_pos exactly as ep_build_send_layout defines them.
+ *   num_worst_rows: rows allocated in the send buffers (T * min(K, P) always
+ *     suffices).  Rows N .. num_worst_rows-1 are left untouched; pass
+ *     num_worst_rows as num_send to ep_dispatch / ep_combine.  If N exceeds it,
+ *     EP_ERR_CAPACITY is set and rows past it are not written (token_pos -1).
+ * Two kernel launches; ws as for ep_compute_send_counts with chunks = 1.
+ * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_COUNT_MISMATCH. */
+int ep_route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
+                    int E_local, int64_t num_worst_rows,
+                    int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                    int32_t *tokens_per_expert,
+                    int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w,
+                    int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
 
 /* [AX] dispatch on the collective-free local path, [UB] Buffer.dispatch
  * payloads: recv_x[n] = x[t] for every (t, p) with n = token_pos[t,p] >= 0.

@@ -323,3 +323,68 @@ def test_batched_duplicate_experts_small():
     assert int(r["err"].item()) == 0
     assert_equal("slot", np_(r["slot"]), o["slot"])
     assert_combine_parity("batched combine", bits16(g_out), o_out)
+
+
+# --------------------------------------------------- no-sync (worst-case) path --
+@pytest.mark.parametrize("name", ["tiny", "mid", "large"])
+def test_route_nosync_matches_oracle(name):
+    w = wl.WORKLOADS[name]
+    x, idx, wts = wl.make(w)
+    o = oracle.send_path(x, idx, wts, None, w.P, w.E_local)
+    N = o["layout"]["n"]
+    y = wl.expert_outputs(w, N)
+    want_out = oracle.combine(y, o["layout"]["token_pos"])
+    dev = "cuda"
+    r = ep.route_nosync(idx.to(dev), wts.to(dev), w.P, w.E_local)
+    W = r["num_worst_rows"]
+    recv = ep.dispatch_rows(x.to(dev), r["token_pos"], W, err=r["err"])
+    y_pad = torch.zeros((W, w.H), dtype=torch.bfloat16, device=dev)
+    y_pad[:N] = y.to(dev)
+    out = ep.combine_rows(y_pad, r["token_pos"], err=r["err"])
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    oc, ol = o["counts"], o["layout"]
+    assert_equal("dest", np_(r["dest"]), oc["dest"])
+    assert_equal("is_in_rank", np_(r["is_in_rank"]), oc["is_in_rank"])
+    assert_equal("send_counts", np_(r["send_counts"]), oc["send_counts"])
+    assert_equal("rank_offsets", np_(r["rank_offsets"]), np.concatenate([[0], np.cumsum(oc["send_counts"])]))
+    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), oc["tokens_per_expert"])
+    for k in ("send_token_idx", "send_rank", "send_idx"):
+        assert_equal(k, np_(r[k])[:N], ol[k])
+    assert_equal("send_w(bits)", np_(r["send_w"])[:N].view(np.uint32), ol["send_w"].view(np.uint32))
+    assert_equal("token_pos", np_(r["token_pos"]), ol["token_pos"])
+    assert_equal("recv_x", bits16(recv)[:N], o["recv_x"])
+    assert_combine_parity("combine", bits16(out), want_out)
+
+
+def test_route_nosync_capacity_is_flagged_and_bounded():
+    T, K, P, El = 700, 4, 4, 4
+    idx, wts = _routing(T, K, P * El, 21)
+    o = oracle.send_path(_randn(T, 8, 1), idx, wts, None, P, El)
+    N = o["layout"]["n"]
+    cap = N - 11
+    dev = "cuda"
+    guard = 8
+    r = ep.route_nosync(idx.to(dev), wts.to(dev), P, El, num_worst_rows=N + guard)   # enough rows
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    assert int(r["rank_offsets"][P].item()) == N
+    # now with too few rows: flagged, nothing past the capacity written
+    sti = torch.full((cap + guard,), -5, dtype=torch.int32, device=dev)
+    sr = torch.full_like(sti, -5)
+    si = torch.full((cap + guard, K), -5, dtype=torch.int64, device=dev)
+    sw = torch.full((cap + guard, K), 9.0, device=dev)
+    outs = dict(dest=torch.empty((T, K), dtype=torch.int32, device=dev),
+                iir=torch.empty((T, P), dtype=torch.uint8, device=dev),
+                sc=torch.empty(P, dtype=torch.int32, device=dev), ro=torch.empty(P + 1, dtype=torch.int32, device=dev),
+                tp=torch.empty((T, P), dtype=torch.int32, device=dev))
+    err = ep.error_word()
+    ep.ep_route_nosync(idx.to(dev), wts.to(dev), T, K, P, El, cap, outs["dest"], outs["iir"], outs["sc"], outs["ro"],
+                       None, sti, sr, si, sw, outs["tp"], ep.workspace(T, K, P, El), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ep.EP_ERR_CAPACITY
+    assert int(outs["ro"][P].item()) == N
+    assert torch.all(sti[cap:] == -5) and torch.all(si[cap:] == -5) and torch.all(sw[cap:] == 9.0)
+    assert int(outs["tp"].max().item()) < cap
+    ol = o["layout"]
+    assert_equal("rows below capacity", np_(sti[:cap]), ol["send_token_idx"][:cap])
