@@ -13,6 +13,7 @@
 // each block's starting offset.  No atomics decide any position, so every
 // index is deterministic and the order is token-ascending by construction.
 #include <algorithm>
+#include <atomic>
 
 #include "ep_device.cuh"
 #include "ep_internal.h"
@@ -565,20 +566,361 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
     return EP_OK;
 }
 
+
+// ------------------------------------------------------- fused route kernel --
+// Counts and send layout in one cooperative launch (all blocks resident at
+// once).  Each thread owns one token and keeps its K expert ids, weights and
+// owning ranks in registers from the counting phase to the layout phase;
+// between the two, every block publishes its per-rank partial counts and an
+// arrival flag, and waits (bounded) until every block's flag carries this
+// call's tag.  Flags from earlier calls carry older tags, so the workspace
+// needs no initialisation.
+constexpr int kFusedThreads = 128;
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr uint64_t kBarrierNs = 500000000ull;   // 0.5 s
+
+struct FusedArgs {
+    const int64_t *idx;
+    const float *w;
+    int64_t T;
+    int K, P, E_local;
+    int64_t num_rows;
+    int32_t *dest;
+    uint8_t *is_in_rank;
+    int32_t *send_counts, *rank_offsets, *tokens_per_expert;
+    int32_t *send_token_idx, *send_rank;
+    int64_t *send_idx;
+    float *send_w;
+    int32_t *token_pos;
+    int32_t *part_rank;       // [gridDim][P]
+    int32_t *part_expert;     // [gridDim][E] when tokens_per_expert is wanted
+    unsigned long long *flags;    // [gridDim]
+    unsigned long long tag;   // non-zero, different for every call
+    int32_t *err;
+};
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// KC > 0: K == KC at compile time (vector row stores); KC == 0: any K <= 32.
+template <int KC>
+__global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
+{
+    constexpr int KM = KC > 0 ? KC : EP_MAX_TOPK;
+    extern __shared__ int32_t s_hist[];          // [E] when counting experts
+    __shared__ int32_t s_warp[kFusedWarps][EP_MAX_RANKS];
+    __shared__ int32_t s_tot[EP_MAX_RANKS], s_before[EP_MAX_RANKS], s_base[EP_MAX_RANKS];
+    __shared__ int s_fail;
+    const int K = KC > 0 ? KC : a.K;
+    const int P = a.P, El = a.E_local, E = P * El;
+    const int b = blockIdx.x, nb = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)b * kFusedThreads + threadIdx.x;
+    const bool valid = t < a.T;
+    const bool want_tpe = a.tokens_per_expert != nullptr;
+
+    // ------------------------------------------------------- counting phase
+    if (want_tpe)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            s_hist[e] = 0;
+    if (threadIdx.x == 0)
+        s_fail = 0;
+    int64_t id[KM];
+    float wt[KM];
+    int8_t dr[KM];
+    uint64_t mask = 0;
+    int bad = 0;
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+        id[k] = -1;
+        wt[k] = 0.0f;
+        dr[k] = -1;
+        if (valid && k < K) {
+            id[k] = a.idx[t * K + k];
+            wt[k] = a.w[t * K + k];
+        }
+    }
+    __syncthreads();   // s_hist zeroed
+    if (valid) {
+#pragma unroll
+        for (int k = 0; k < KM; ++k) {
+            if (k >= K)
+                break;
+            const int64_t e = id[k];
+            int d = -1;
+            if (e >= 0 && e < E)
+                d = (int)(e / El);
+            else if (e != -1)
+                bad = EP_ERR_INVALID_EXPERT;
+            dr[k] = (int8_t)d;
+            a.dest[t * K + k] = d;
+            if (d >= 0) {
+                mask |= 1ull << d;
+                if (want_tpe) {
+                    bool seen = false;
+#pragma unroll
+                    for (int j = 0; j < KM; ++j)
+                        seen |= (j < k && id[j] == e);
+                    if (!seen)
+                        atomicAdd(&s_hist[e], 1);
+                }
+            }
+        }
+        uint8_t *irow = a.is_in_rank + t * P;
+        if ((P & 3) == 0) {
+            for (int p = 0; p < P; p += 4)
+                *reinterpret_cast<uint32_t *>(irow + p) =
+                    (uint32_t)((mask >> p) & 1ull) | (uint32_t)((mask >> (p + 1)) & 1ull) << 8 |
+                    (uint32_t)((mask >> (p + 2)) & 1ull) << 16 | (uint32_t)((mask >> (p + 3)) & 1ull) << 24;
+        } else {
+            for (int p = 0; p < P; ++p)
+                irow[p] = (uint8_t)((mask >> p) & 1ull);
+        }
+    }
+    for (int p = 0; p < P; ++p) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+        if (lane == 0)
+            s_warp[warp][p] = __popc(bal);
+    }
+    __syncthreads();
+    if (threadIdx.x < P) {
+        int run = 0;
+        for (int ww = 0; ww < kFusedWarps; ++ww) {
+            const int v = s_warp[ww][threadIdx.x];
+            s_warp[ww][threadIdx.x] = run;          // exclusive prefix over this block's warps
+            run += v;
+        }
+        a.part_rank[(int64_t)b * P + threadIdx.x] = run;
+    }
+    if (want_tpe)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            a.part_expert[(int64_t)b * E + e] = s_hist[e];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        st_release_u64(&a.flags[b], a.tag);
+    }
+
+    // -------------------------------------------------------- grid barrier
+    {
+        bool ok = true;
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+            if (ld_acquire_u64(&a.flags[i]) == a.tag)
+                continue;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_u64(&a.flags[i]) != a.tag) {
+                if (global_timer_ns() - t0 > kBarrierNs) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok)
+                break;
+        }
+        if (!ok)
+            s_fail = 1;
+        __threadfence();
+        __syncthreads();
+        if (s_fail) {
+            if (threadIdx.x == 0)
+                raise(a.err, EP_ERR_TIMEOUT);
+            return;   // the whole block leaves together
+        }
+    }
+
+    // --------------------------------------------------------- layout phase
+    if (threadIdx.x < P) {
+        s_tot[threadIdx.x] = 0;
+        s_before[threadIdx.x] = 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb * P; i += blockDim.x) {
+        const int v = a.part_rank[i];
+        const int bb = i / P, p = i - bb * P;
+        atomicAdd(&s_tot[p], v);
+        if (bb < b)
+            atomicAdd(&s_before[p], v);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int v0 = lane < P ? s_tot[lane] : 0;
+        const int v1 = lane + 32 < P ? s_tot[lane + 32] : 0;
+        int e0, e1;
+        const int grand = warp_exclusive_scan64(v0, v1, e0, e1);
+        if (lane < P)
+            s_base[lane] = e0 + s_before[lane];
+        if (lane + 32 < P)
+            s_base[lane + 32] = e1 + s_before[lane + 32];
+        if (b == 0) {
+            if (lane < P) {
+                a.send_counts[lane] = v0;
+                a.rank_offsets[lane] = e0;
+            }
+            if (lane + 32 < P) {
+                a.send_counts[lane + 32] = v1;
+                a.rank_offsets[lane + 32] = e1;
+            }
+            if (lane == 0) {
+                a.rank_offsets[P] = grand;
+                if ((int64_t)grand > a.num_rows)
+                    raise(a.err, EP_ERR_CAPACITY);
+            }
+        }
+    }
+    if (want_tpe) {
+        // experts b, b + nb, ...: one partial per thread and step
+        const int mine = (E - b + nb - 1) / nb;
+        for (int j0 = 0; j0 < mine; j0 += E) {
+            for (int j = threadIdx.x; j < mine; j += blockDim.x)
+                s_hist[j] = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < mine * nb; i += blockDim.x) {
+                const int j = i / nb, bb = i - j * nb;
+                atomicAdd(&s_hist[j], a.part_expert[(int64_t)bb * E + b + j * nb]);
+            }
+            __syncthreads();
+            for (int j = threadIdx.x; j < mine; j += blockDim.x)
+                a.tokens_per_expert[b + j * nb] = s_hist[j];
+        }
+    }
+    __syncthreads();
+
+    if (valid) {
+        int32_t *tp = a.token_pos + t * P;
+        for (int p = 0; p < P; ++p)
+            tp[p] = -1;
+    }
+    for (int p = 0; p < P; ++p) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+        if (!((mask >> p) & 1ull))
+            continue;
+        const int64_t n = (int64_t)s_base[p] + s_warp[warp][p] + __popc(bal & lanemask_lt());
+        if (n >= a.num_rows) {
+            bad = EP_ERR_CAPACITY;
+            continue;
+        }
+        a.token_pos[t * P + p] = (int32_t)n;
+        a.send_token_idx[n] = (int32_t)t;
+        a.send_rank[n] = p;
+        const int64_t off = (int64_t)p * El;
+        int64_t *si = a.send_idx + n * K;
+        float *sw = a.send_w + n * K;
+        if (KC > 0 && (KC & 1) == 0) {
+#pragma unroll
+            for (int k = 0; k < KM; k += 2) {
+                const longlong2 v = make_longlong2(dr[k] == p ? id[k] - off : -1, dr[k + 1] == p ? id[k + 1] - off : -1);
+                *reinterpret_cast<longlong2 *>(si + k) = v;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < KM; ++k)
+                if (k < K)
+                    si[k] = dr[k] == p ? id[k] - off : -1;
+        }
+        if (KC > 0 && (KC & 3) == 0) {
+#pragma unroll
+            for (int k = 0; k < KM; k += 4)
+                *reinterpret_cast<float4 *>(sw + k) =
+                    make_float4(dr[k] == p ? wt[k] : 0.0f, dr[k + 1] == p ? wt[k + 1] : 0.0f,
+                                dr[k + 2] == p ? wt[k + 2] : 0.0f, dr[k + 3] == p ? wt[k + 3] : 0.0f);
+        } else {
+#pragma unroll
+            for (int k = 0; k < KM; ++k)
+                if (k < K)
+                    sw[k] = dr[k] == p ? wt[k] : 0.0f;
+        }
+    }
+    raise(a.err, bad);
+}
+
+template <int KC>
+static int launch_route_fused(const FusedArgs &a, int nb, size_t smem, cudaStream_t stream, bool *launched)
+{
+    *launched = false;
+    static int max_per_sm[2] = {-1, -1};   // [counting experts?]
+    const int slot = smem > 0 ? 1 : 0;
+    if (max_per_sm[slot] < 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_fused_kernel<KC>, kFusedThreads, smem) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        max_per_sm[slot] = n;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_OK;
+    }
+    if ((int64_t)max_per_sm[slot] * sms < nb)
+        return EP_OK;   // cannot be co-resident: the caller falls back to two launches
+    FusedArgs copy = a;
+    void *args[] = {&copy};
+    if (cudaLaunchCooperativeKernel((const void *)route_fused_kernel<KC>, dim3(nb), dim3(kFusedThreads), args, smem,
+                                    stream) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    *launched = true;
+    return EP_OK;
+}
+
+static unsigned long long next_route_tag()
+{
+    static std::atomic<unsigned long long> epoch{0x9e3779b97f4a7c15ull};
+    unsigned long long v;
+    do {
+        v = epoch.fetch_add(0x632be59bd9b4e019ull);
+    } while (v == 0);
+    return v;
+}
 }  // namespace ep
 
 // ================================================================ C ABI ====
 using namespace ep;
+
+// Workspace regions shared by the routing calls (sized for routing blocks of
+// 128 tokens, twice as many as the 256-token blocks most kernels use):
+// per-block rank counts, per-block expert counts, per-block arrival flags.
+struct WsLayout {
+    int32_t *part_rank;
+    int32_t *part_expert;
+    unsigned long long *flags;
+};
+
+static size_t ws_blocks(int64_t T, int chunks) { return 2 * (size_t)route_blocks_max(T, chunks); }
+
+static WsLayout ws_layout(void *ws, int64_t T, int chunks, int P, int E)
+{
+    const size_t nb = ws_blocks(T, chunks);
+    char *base = static_cast<char *>(ws);
+    WsLayout l;
+    l.part_rank = reinterpret_cast<int32_t *>(base);
+    base += align_up(nb * P * sizeof(int32_t), kWsAlign);
+    l.part_expert = reinterpret_cast<int32_t *>(base);
+    base += align_up(nb * E * sizeof(int32_t), kWsAlign);
+    l.flags = reinterpret_cast<unsigned long long *>(base);
+    return l;
+}
 
 extern "C" size_t ep_workspace_size(int64_t T, int K, int P, int E_local, int chunks)
 {
     (void)K;
     if (T < 0 || P < 1 || E_local < 1)
         return 0;
-    const int64_t nb = route_blocks_max(T, chunks);
-    const int64_t E = (int64_t)P * E_local;
-    return align_up((size_t)nb * P * sizeof(int32_t), kWsAlign) +
-           align_up((size_t)nb * E * sizeof(int32_t), kWsAlign);
+    const size_t nb = ws_blocks(T, chunks);
+    const size_t E = (size_t)P * E_local;
+    return align_up(nb * P * sizeof(int32_t), kWsAlign) + align_up(nb * E * sizeof(int32_t), kWsAlign) +
+           align_up(nb * sizeof(unsigned long long), kWsAlign);
 }
 
 extern "C" int ep_chunk_bounds(int64_t T, int chunks, int64_t *h_bounds)
@@ -640,11 +982,9 @@ extern "C" int ep_compute_send_counts(const int64_t *topk_idx, int64_t T, int K,
     ct.first_block[C] = nb;
 
     const int E = P * E_local;
-    const int64_t nb_max = route_blocks_max(T, chunks);
-    int32_t *part_rank = static_cast<int32_t *>(ws);
-    int32_t *part_expert = reinterpret_cast<int32_t *>(
-        static_cast<char *>(ws) + align_up((size_t)nb_max * P * sizeof(int32_t), kWsAlign));
-    int32_t *pe = tokens_per_expert != nullptr ? part_expert : nullptr;
+    const WsLayout wl = ws_layout(ws, T, chunks, P, E);
+    int32_t *part_rank = wl.part_rank;
+    int32_t *pe = tokens_per_expert != nullptr ? wl.part_expert : nullptr;
 
     if (nb > 0) {
         const size_t smem = sizeof(int32_t) * (kWarps * P + (pe != nullptr ? E : 0));
@@ -708,31 +1048,49 @@ extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weight
     if (num_worst_rows > 0 && (send_token_idx == nullptr || send_rank == nullptr || send_idx == nullptr ||
                                send_w == nullptr))
         return EP_ERR_INVALID_ARG;
-    const int nb = (int)ceil_div(T, kRouteThreads);
     const int E = P * E_local;
-    int32_t *part_rank = static_cast<int32_t *>(ws);
-    int32_t *part_expert = reinterpret_cast<int32_t *>(
-        static_cast<char *>(ws) + align_up((size_t)route_blocks_max(T, 1) * P * sizeof(int32_t), kWsAlign));
-    if (nb == 0) {   // nothing routed: zero counts through the single-chunk finish
+    const WsLayout wl = ws_layout(ws, T, 1, P, E);
+    int32_t *pe = tokens_per_expert != nullptr ? wl.part_expert : nullptr;
+    if (T == 0) {   // nothing routed: zero counts through the single-chunk finish
         ChunkTable ct{};
         ct.n = 1;
-        count_finish_kernel<<<1, 1024, 0, stream>>>(part_rank, nullptr, 0, P, E, ct, send_counts, rank_offsets,
+        count_finish_kernel<<<1, 1024, 0, stream>>>(wl.part_rank, nullptr, 0, P, E, ct, send_counts, rank_offsets,
                                                     tokens_per_expert);
         return launch_status();
     }
+
+    // one cooperative launch when every block can be resident at once
+    const int nbf = (int)ceil_div(T, kFusedThreads);
+    const size_t smem_f = pe != nullptr ? sizeof(int32_t) * E : 0;
+    FusedArgs fa{topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
+                 rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos,
+                 wl.part_rank, pe, wl.flags, next_route_tag(), err};
+    bool launched = false;
+    int rc;
+    switch (K) {
+    case 2: rc = launch_route_fused<2>(fa, nbf, smem_f, stream, &launched); break;
+    case 4: rc = launch_route_fused<4>(fa, nbf, smem_f, stream, &launched); break;
+    case 6: rc = launch_route_fused<6>(fa, nbf, smem_f, stream, &launched); break;
+    case 8: rc = launch_route_fused<8>(fa, nbf, smem_f, stream, &launched); break;
+    default: rc = launch_route_fused<0>(fa, nbf, smem_f, stream, &launched); break;
+    }
+    if (rc != EP_OK || launched)
+        return rc;
+
+    // otherwise: count_kernel, then layout_write_kernel from its partials
+    const int nb = (int)ceil_div(T, kRouteThreads);
     ChunkTable ct{};
     ct.n = 1;
     ct.start[0] = 0;
     ct.start[1] = T;
     ct.first_block[0] = 0;
     ct.first_block[1] = nb;
-    int32_t *pe = tokens_per_expert != nullptr ? part_expert : nullptr;
     const size_t smem = sizeof(int32_t) * (kWarps * P + (pe != nullptr ? E : 0));
-    count_kernel<<<nb, kRouteThreads, smem, stream>>>(topk_idx, K, P, E_local, ct, dest, is_in_rank, part_rank, pe,
-                                                      err);
+    count_kernel<<<nb, kRouteThreads, smem, stream>>>(topk_idx, K, P, E_local, ct, dest, is_in_rank, wl.part_rank,
+                                                      pe, err);
     if (launch_status() != EP_OK)
         return EP_ERR_CUDA;
-    LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_worst_rows, 0, part_rank, nb,
+    LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_worst_rows, 0, wl.part_rank, nb,
                  pe, send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
                  token_pos, err};
     layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);

@@ -388,3 +388,47 @@ def test_route_nosync_capacity_is_flagged_and_bounded():
     assert int(outs["tp"].max().item()) < cap
     ol = o["layout"]
     assert_equal("rows below capacity", np_(sti[:cap]), ol["send_token_idx"][:cap])
+
+
+@pytest.mark.parametrize("T,H,K,P,E_local,fu,dup", EDGE)
+def test_route_nosync_edges(T, H, K, P, E_local, fu, dup):
+    idx, wts = _routing(T, K, P * E_local, seed=T + H + 1, frac_unrouted=fu, dup=dup)
+    o = oracle.send_path(_randn(T, 8, 2), idx, wts, None, P, E_local)
+    N = o["layout"]["n"]
+    dev = "cuda"
+    r = ep.route_nosync(idx.to(dev), wts.to(dev), P, E_local)
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    oc, ol = o["counts"], o["layout"]
+    assert_equal("dest", np_(r["dest"]), oc["dest"])
+    assert_equal("is_in_rank", np_(r["is_in_rank"]), oc["is_in_rank"])
+    assert_equal("send_counts", np_(r["send_counts"]), oc["send_counts"])
+    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), oc["tokens_per_expert"])
+    assert int(r["rank_offsets"][P].item()) == N
+    for k in ("send_token_idx", "send_rank", "send_idx"):
+        assert_equal(k, np_(r[k])[:N], ol[k])
+    assert_equal("send_w(bits)", np_(r["send_w"])[:N].view(np.uint32), ol["send_w"].view(np.uint32))
+    assert_equal("token_pos", np_(r["token_pos"]), ol["token_pos"])
+
+
+def test_route_nosync_repeated_calls_reuse_workspace():
+    # back-to-back calls on one workspace: each call's arrival flags carry a
+    # new tag, so the previous call's flags never satisfy the barrier
+    w = wl.WORKLOADS["mid"]
+    idx, wts = wl.routing(w)
+    dev = "cuda"
+    ws = ep.workspace(w.T, w.K, w.P, w.E_local)
+    first = ep.route_nosync(idx.to(dev), wts.to(dev), w.P, w.E_local, ws=ws)
+    idx2 = idx.clone()
+    idx2[:, 0] = -1
+    second = ep.route_nosync(idx2.to(dev), wts.to(dev), w.P, w.E_local, ws=ws)
+    third = ep.route_nosync(idx.to(dev), wts.to(dev), w.P, w.E_local, ws=ws)
+    torch.cuda.synchronize()
+    o2 = oracle.compute_send_counts(idx2, w.P, w.E_local)
+    assert_equal("second send_counts", np_(second["send_counts"]), o2["send_counts"])
+    N = int(first["rank_offsets"][w.P].item())
+    for k in ("send_counts", "rank_offsets", "token_pos"):
+        assert torch.equal(first[k], third[k]), k
+    for k in ("send_token_idx", "send_rank", "send_idx", "send_w"):   # rows past N are not written
+        assert torch.equal(first[k][:N], third[k][:N]), k
+    assert int(first["err"].item()) == int(second["err"].item()) == int(third["err"].item()) == 0
