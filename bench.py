@@ -75,28 +75,35 @@ def measured_peak() -> tuple:
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def kernel_source_hash() -> str:
+# Source files of the kernels whose DRAM traffic profiles/traffic.json records.
+KERNEL_SOURCES = {
+    "dispatch": ["ep_move.cu", "ep_rows.cuh", "ep_device.cuh", "ep_internal.h"],
+    "combine": ["ep_combine.cu", "ep_rows.cuh", "ep_device.cuh", "ep_internal.h"],
+    "route": ["ep_route.cu", "ep_device.cuh", "ep_internal.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_send_counts_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel] + ["../../include/ep.h"]:
         with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+            h.update(os.path.basename(name).encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; otherwise None."""
+    """DRAM bytes per full-size launch from the committed ncu capture, if it was
+    taken on the kernel's current sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
+            k = json.load(f)["kernels"][kernel]
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash():
+    if k.get("source_hash") != kernel_source_hash(kernel):
         return None
-    k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_launch_full_size")
+    return k.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
