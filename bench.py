@@ -185,6 +185,7 @@ class SendPath:
         self.rank_offsets = torch.empty((1, P + 1), dtype=i32, device=dev)
         self.counts_h = torch.empty((1, P), dtype=i32, pin_memory=True)
         self.ws = ep.workspace(T, K, P, El, 1, dev)
+        self.cws = ep.combine_ws(dev)
         self.err = ep.error_word(dev)
         self.token_pos = torch.empty((T, P), dtype=i32, device=dev)
         self.N = None
@@ -215,7 +216,7 @@ class SendPath:
         ep.ep_dispatch(self.x, T, H, self.token_pos, P, W, self.recv_x, None, 0, self.err, stream)
         if ev is not None:
             ev[2].record(stream)
-        ep.ep_combine(y, T, H, self.token_pos, P, W, self.out, 0, self.err, stream)
+        ep.ep_combine(y, T, H, self.token_pos, P, W, self.out, 0, self.cws, self.err, stream)
         if ev is not None:
             ev[3].record(stream)
 
@@ -240,7 +241,7 @@ class SendPath:
         rec(3)
         ep.ep_dispatch(self.x, T, H, self.token_pos, P, num_send, self.recv_x, None, 0, self.err, stream)
         rec(4)
-        ep.ep_combine(y, T, H, self.token_pos, P, num_send, self.out, 0, self.err, stream)
+        ep.ep_combine(y, T, H, self.token_pos, P, num_send, self.out, 0, self.cws, self.err, stream)
         rec(5)
 
 

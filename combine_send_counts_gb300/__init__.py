@@ -61,10 +61,11 @@ _SIGNATURES = {
     "ep_build_send_layout": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I64, _VP, _VP, _VP, _VP,
                                     _VP, _VP, _SZ, _VP, _VP]),
     "ep_dispatch": (_I32, [_VP, _I64, _I32, _VP, _I32, _I64, _VP, _VP, _I32, _VP, _VP]),
-    "ep_combine": (_I32, [_VP, _I64, _I32, _VP, _I32, _I64, _VP, _I32, _VP, _VP]),
+    "ep_combine": (_I32, [_VP, _I64, _I32, _VP, _I32, _I64, _VP, _I32, _VP, _SZ, _VP, _VP]),
     "ep_batched_prepare": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32,
                                   _VP, _SZ, _VP, _VP]),
-    "ep_batched_combine": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "ep_batched_combine": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _SZ, _VP,
+                                  _VP]),
     "ep_local_expert_fp8": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP]),
     "ep_route_nosync": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                _VP, _VP, _VP, _SZ, _VP, _VP]),
@@ -169,9 +170,13 @@ def ep_dispatch(x, T, H, token_pos, P, num_send, recv_x, recv_scale, fp8, err, s
     _check(rc, "ep_dispatch")
 
 
-def ep_combine(y, T, H, token_pos, P, num_send, out, out_dtype, err, stream=None):
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def ep_combine(y, T, H, token_pos, P, num_send, out, out_dtype, ws, err, stream=None):
     rc = load().ep_combine(_p(y), int(T), int(H), _p(token_pos), int(P), int(num_send), _p(out),
-                           int(out_dtype), _p(err), _stream(stream))
+                           int(out_dtype), _p(ws), _nbytes(ws), _p(err), _stream(stream))
     _check(rc, "ep_combine")
 
 
@@ -184,11 +189,11 @@ def ep_batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b
     _check(rc, "ep_batched_prepare")
 
 
-def ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, E_local, rank, max_num_tokens, out, err,
+def ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, E_local, rank, max_num_tokens, out, ws, err,
                        stream=None):
     rc = load().ep_batched_combine(_p(y), _p(topk_idx), _p(topk_weights), _p(slot), int(T), int(K), int(H),
-                                   int(E_local), int(rank), int(max_num_tokens), _p(out), _p(err),
-                                   _stream(stream))
+                                   int(E_local), int(rank), int(max_num_tokens), _p(out), _p(ws), _nbytes(ws),
+                                   _p(err), _stream(stream))
     _check(rc, "ep_batched_combine")
 
 
@@ -327,12 +332,23 @@ def dispatch_rows(x: torch.Tensor, token_pos: torch.Tensor, num_send: int, fp8: 
     return recv
 
 
-def combine_rows(y: torch.Tensor, token_pos: torch.Tensor, out_dtype=torch.bfloat16, err=None, stream=None):
+EP_COMBINE_WS_BYTES = 16
+
+
+def combine_ws(device=None) -> torch.Tensor:
+    """Scratch for ep_combine / ep_batched_combine (lets the SMs share work)."""
+    return torch.empty(256, dtype=torch.uint8, device=device or "cuda")
+
+
+def combine_rows(y: torch.Tensor, token_pos: torch.Tensor, out_dtype=torch.bfloat16, err=None, stream=None,
+                 ws="auto"):
+    """ws: "auto" (a fresh scratch), a device tensor, or None (static work split)."""
     T, P = token_pos.shape
     N, H = y.shape
     out = torch.empty((T, H), dtype=out_dtype, device=y.device)
     err = err if err is not None else error_word(y.device)
-    ep_combine(y, T, H, token_pos, P, N, out, 1 if out_dtype == torch.float32 else 0, err, stream)
+    ws = combine_ws(y.device) if isinstance(ws, str) else ws
+    ep_combine(y, T, H, token_pos, P, N, out, 1 if out_dtype == torch.float32 else 0, ws, err, stream)
     return out
 
 
@@ -370,12 +386,13 @@ def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank:
     return dict(b_x=b_x, tokens_per_expert=tpe, slot=slot, err=err)
 
 
-def batched_combine(y, topk_idx, topk_weights, slot, rank: int, err=None, stream=None):
+def batched_combine(y, topk_idx, topk_weights, slot, rank: int, err=None, stream=None, ws="auto"):
     El, M, H = y.shape
     T, K = topk_idx.shape
     out = torch.empty((T, H), dtype=y.dtype, device=y.device)
     err = err if err is not None else error_word(y.device)
-    ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, El, rank, M, out, err, stream)
+    ws = combine_ws(y.device) if isinstance(ws, str) else ws
+    ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, El, rank, M, out, ws, err, stream)
     return out
 
 

@@ -38,7 +38,6 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kGatherThreads = 32 + kConsumers;
 constexpr int kQueue = 16;          // descriptor slots: how far the producer may run ahead in items
-constexpr int kBatch = 32;          // items whose source lists the producer resolves at once
 constexpr int kVMax = 4;            // 16-byte vectors per consumer thread per chunk
 constexpr int kMaxChunkCols = kConsumers * kVMax * 8;   // 8192 bf16 columns = 16 KB per buffer
 constexpr int kMaxBuffers = 64;
@@ -49,7 +48,7 @@ constexpr uint64_t kDrainNs = 50000000ull;        // 50 ms per buffer when drain
 struct Desc {
     int64_t t;
     int32_t c;
-    int32_t nsrc;
+    int32_t nsrc;       // -1 ends the sequence
     float w[kMaxList];
 };
 
@@ -60,21 +59,25 @@ struct GatherGeom {
     int B;          // ring buffers, a power of two
     int logB;       // log2(B): buffer of use u is u & (B-1), its phase parity (u >> logB) & 1
     int RB;         // bytes per ring buffer (multiple of 128)
+    int lpi;        // lanes of the producer warp per item (8, 16 or 32)
+    int cb;         // items per claim (32 / lpi)
 };
 
-__host__ __device__ inline size_t gather_smem_bytes(const GatherGeom &g, int D)
+__host__ __device__ inline size_t gather_smem_bytes(const GatherGeom &g)
 {
     return (size_t)g.B * g.RB                       // ring
            + sizeof(uint64_t) * (2 * g.B + 2 * kQueue)   // mbarriers
            + sizeof(int64_t) * g.B                   // last armed use per buffer
-           + sizeof(Desc) * kQueue                   // descriptor queue
-           + (sizeof(int32_t) + sizeof(float)) * kBatch * D + sizeof(int32_t) * kBatch;   // lists
+           + sizeof(Desc) * kQueue;                  // descriptor queue
 }
 
+// counter: NULL for a static round-robin of claims over the CTAs, or a
+// device word set to 0 before the launch, from which the producers claim
+// their next items (balances skewed source counts).
 template <class Rows, bool WEIGHTED, bool OUT_F32>
 __global__ void __launch_bounds__(kGatherThreads, 1)
 gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows rows, int64_t n_rows,
-                  int err_bits, void *__restrict__ out, int32_t *err)
+                  int err_bits, void *__restrict__ out, unsigned int *counter, int32_t *err)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int D = rows.len();
@@ -85,9 +88,6 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
     uint64_t *qempty = qfull + kQueue;
     int64_t *last_use = reinterpret_cast<int64_t *>(qempty + kQueue);
     Desc *desc = reinterpret_cast<Desc *>(last_use + g.B);
-    int32_t *l_row = reinterpret_cast<int32_t *>(desc + kQueue);
-    float *l_w = reinterpret_cast<float *>(l_row + kBatch * D);
-    int32_t *l_n = reinterpret_cast<int32_t *>(l_w + kBatch * D);
     __shared__ int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,107 +108,162 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
 
     volatile int *abort_flag = &s_abort;
     const int n_items = (int)(T * g.nchunk);   // < 2^31, checked on the host
-    const int stride = gridDim.x;
     int bad = 0;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
+        // Lane l serves item l / lpi of a claim and source slots j0 = l % lpi
+        // and j0 + 32 (lists longer than 32).
+        const int my_i = lane / g.lpi, j0 = lane % g.lpi, j1 = j0 + 32;
+        const unsigned item_lanes = (g.lpi == 32 ? kFull : ((1u << g.lpi) - 1u)) << (my_i * g.lpi);
+        uint32_t static_k = 0;
+        auto claim = [&]() -> int {
+            if (counter == nullptr)
+                return (int)((blockIdx.x + (static_k++) * gridDim.x) * (uint32_t)g.cb);
+            int c = 0;
+            if (lane == 0)
+                c = (int)atomicAdd(counter, (unsigned)g.cb);
+            return __shfl_sync(kFull, c, 0);
+        };
+        auto load = [&](int base, typename Rows::Raw &r0, typename Rows::Raw &r1, bool &v0, bool &v1) {
+            const int item = base + my_i;
+            v0 = false;
+            v1 = false;
+            if (item < n_items) {
+                const int64_t t = g.nchunk == 1 ? item : item / g.nchunk;
+                v0 = j0 < D;
+                v1 = j1 < D;
+                if (v0)
+                    r0 = rows.load(t, j0);
+                if (v1)
+                    r1 = rows.load(t, j1);
+            }
+        };
+
         uint32_t use = 0;  // buffer uses armed so far (warp-uniform)
-        uint32_t k = 0;    // items published so far
-        for (int i0 = blockIdx.x; i0 < n_items && !*abort_flag; i0 += stride * kBatch) {
-            // lane l resolves the source list of item i0 + l * stride
-            const int mine = i0 + lane * stride;
-            int n = 0;
-            if (mine < n_items) {
-                const int64_t t = g.nchunk == 1 ? mine : mine / g.nchunk;
-                for (int j0 = 0; j0 < D; j0 += 8) {
-                    int32_t r8[8];
-                    float w8[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = j0 + jj;
-                        r8[jj] = j < D ? rows.row(t, j) : -1;
-                        w8[jj] = (WEIGHTED && j < D) ? rows.weight(t, j) : 1.0f;
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        int32_t r = r8[jj];
-                        if (r >= n_rows) {
-                            bad = err_bits;
-                            r = -1;
-                        }
-                        if (r >= 0) {
-                            l_row[lane * D + n] = r;
-                            l_w[lane * D + n] = w8[jj];
-                            ++n;
-                        }
-                    }
+        uint32_t k = 0;    // descriptors published so far
+        typename Rows::Raw rc0{}, rc1{}, rn0{}, rn1{};
+        bool vc0, vc1, vn0, vn1;
+        int c_cur = claim();
+        int c_nxt = claim();
+        load(c_cur, rc0, rc1, vc0, vc1);
+        while (c_cur < n_items && !*abort_flag) {
+            const int c_aft = claim();
+            load(c_nxt, rn0, rn1, vn0, vn1);          // used by the next claim
+            bool ok = true;
+            int32_t r0 = -1, r1 = -1;
+            if (vc0) {
+                r0 = rows.decode(rc0);
+                if (r0 >= n_rows) {
+                    bad = err_bits;
+                    r0 = -1;
                 }
             }
-            l_n[lane] = n;
-            __syncwarp();
-            const int left = (n_items - i0 + stride - 1) / stride;
-            const int nb = left < kBatch ? left : kBatch;
-            for (int bi = 0; bi < nb; ++bi, ++k) {
-                const int item = i0 + bi * stride;
-                const int nsrc = l_n[bi];
+            if (vc1) {
+                r1 = rows.decode(rc1);
+                if (r1 >= n_rows) {
+                    bad = err_bits;
+                    r1 = -1;
+                }
+            }
+            const float w0 = WEIGHTED && vc0 ? rows.weight(rc0) : 1.0f;
+            const float w1 = WEIGHTED && vc1 ? rows.weight(rc1) : 1.0f;
+            const unsigned bal0 = __ballot_sync(kFull, r0 >= 0);
+            const unsigned bal1 = __ballot_sync(kFull, r1 >= 0);
+            for (int i = 0; i < g.cb && ok; ++i) {
+                const int item = c_cur + i;
+                if (item >= n_items)
+                    break;
+                const unsigned m = (g.lpi == 32 ? kFull : ((1u << g.lpi) - 1u)) << (i * g.lpi);
+                const int n0 = __popc(bal0 & m), nsrc = n0 + __popc(bal1 & m);
+                const bool mine = item_lanes == m;
                 const int q = (int)(k % kQueue);
-                bool ok = true;
                 if (lane == 0 && k >= kQueue)
                     ok = mbar_wait(&qempty[q], ((k / kQueue) - 1) & 1, kWaitNs);
-                if (!__all_sync(kFull, ok)) {
-                    bad |= EP_ERR_TIMEOUT;
-                    *abort_flag = 1;
+                ok = __all_sync(kFull, ok);
+                if (!ok)
                     break;
-                }
                 const int chunk = g.nchunk == 1 ? 0 : item % g.nchunk;
                 if (lane == 0) {
                     desc[q].t = g.nchunk == 1 ? item : item / g.nchunk;
                     desc[q].c = chunk;
                     desc[q].nsrc = nsrc;
                 }
-                for (int o = lane; o < nsrc; o += 32)
-                    desc[q].w[o] = l_w[bi * D + o];
+                const int o0 = __popc(bal0 & m & lanemask_lt());
+                const int o1 = n0 + __popc(bal1 & m & lanemask_lt());
+                if (WEIGHTED && mine) {
+                    if (r0 >= 0)
+                        desc[q].w[o0] = w0;
+                    if (r1 >= 0)
+                        desc[q].w[o1] = w1;
+                }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&qfull[q]);
+                ++k;
                 const int col0 = chunk * g.CH;
                 const uint32_t bytes = (uint32_t)min(g.CH, g.H - col0) * 2u;
-                for (int o = lane; o < nsrc; o += 32) {
-                    const uint32_t u = use + o;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t r = h == 0 ? r0 : r1;
+                    if (!mine || r < 0)
+                        continue;
+                    const uint32_t u = use + (h == 0 ? o0 : o1);
                     const int b = (int)(u & (g.B - 1));
                     if (u >= (uint32_t)g.B && !mbar_wait(&empty[b], ((u >> g.logB) - 1) & 1, kWaitNs)) {
                         ok = false;
                         continue;
                     }
                     mbar_arrive_expect_tx(&full[b], bytes);
-                    bulk_g2s(ring + (size_t)b * g.RB,
-                             y + ((int64_t)l_row[bi * D + o] * g.H + col0) * 2, bytes, &full[b]);
+                    bulk_g2s(ring + (size_t)b * g.RB, y + ((int64_t)r * g.H + col0) * 2, bytes, &full[b]);
                     last_use[b] = u;
                 }
                 use += nsrc;
-                if (!__all_sync(kFull, ok)) {
-                    bad |= EP_ERR_TIMEOUT;
-                    *abort_flag = 1;
-                    break;
-                }
+                ok = __all_sync(kFull, ok);
             }
-            __syncwarp();
+            if (!ok) {
+                bad |= EP_ERR_TIMEOUT;
+                *abort_flag = 1;
+                break;
+            }
+            c_cur = c_nxt;
+            c_nxt = c_aft;
+            rc0 = rn0;
+            rc1 = rn1;
+            vc0 = vn0;
+            vc1 = vn1;
+        }
+        // end of the sequence for the consumers
+        if (!*abort_flag) {
+            const int q = (int)(k % kQueue);
+            bool ok = true;
+            if (lane == 0 && k >= kQueue)
+                ok = mbar_wait(&qempty[q], ((k / kQueue) - 1) & 1, kWaitNs);
+            if (lane == 0 && ok) {
+                desc[q].nsrc = -1;
+                mbar_arrive(&qfull[q]);
+            }
+            if (!__all_sync(kFull, ok)) {
+                bad |= EP_ERR_TIMEOUT;
+                *abort_flag = 1;
+            }
         }
     } else {
         // --------------------------------------------------------- consumers
         const int ct = threadIdx.x - 32;
         uint32_t use = 0, k = 0;
-        for (int item = blockIdx.x; item < n_items; item += stride, ++k) {
+        while (true) {
             const int q = (int)(k % kQueue);
             if (*abort_flag || !mbar_wait(&qfull[q], (k / kQueue) & 1, kWaitNs)) {
                 bad |= *abort_flag ? 0 : EP_ERR_TIMEOUT;
                 *abort_flag = 1;
                 break;
             }
+            const int nsrc = desc[q].nsrc;
+            if (nsrc < 0)
+                break;
             const int64_t t = desc[q].t;
             const int col0 = desc[q].c * g.CH;
-            const int nsrc = desc[q].nsrc;
             const int nv = min(g.CH, g.H - col0) / 8;
             float acc[kVMax][8];
 #pragma unroll
@@ -270,6 +325,7 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&qempty[q]);
+            ++k;
         }
     }
 
@@ -303,12 +359,12 @@ static GatherGeom gather_geometry(int H, int D)
     g.nchunk = (int)ceil_div(H, kMaxChunkCols);
     g.CH = (int)align_up((size_t)ceil_div(H, g.nchunk), 8);
     g.RB = (int)align_up((size_t)g.CH * 2, 128);
-    g.B = 1;
-    GatherGeom probe = g;
-    probe.B = 0;
-    const size_t fixed = gather_smem_bytes(probe, D);
-    const size_t fit = std::min<size_t>(kMaxBuffers, (kSmemBudget - fixed) / (g.RB + 2 * sizeof(uint64_t) + sizeof(int64_t)));
+    g.lpi = D <= 8 ? 8 : D <= 16 ? 16 : 32;
+    g.cb = 32 / g.lpi;
+    g.B = 0;
     g.logB = 0;
+    const size_t fixed = gather_smem_bytes(g);
+    const size_t fit = std::min<size_t>(kMaxBuffers, (kSmemBudget - fixed) / (g.RB + 2 * sizeof(uint64_t) + sizeof(int64_t)));
     while ((size_t)(2 << g.logB) <= fit)
         ++g.logB;
     g.B = 1 << g.logB;
@@ -317,11 +373,11 @@ static GatherGeom gather_geometry(int H, int D)
 
 template <class Rows, bool WEIGHTED, bool OUT_F32>
 static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, int64_t n_rows, int err_bits,
-                             void *out, int32_t *err, cudaStream_t stream)
+                             void *out, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream)
 {
     const int D = rows.len();
     const GatherGeom g = gather_geometry(H, D);
-    const size_t smem = gather_smem_bytes(g, D);
+    const size_t smem = gather_smem_bytes(g);
     auto kernel = gather_tma_kernel<Rows, WEIGHTED, OUT_F32>;
     static size_t smem_set = 0;   // per instantiation; raising the limit is idempotent
     if (smem > smem_set) {
@@ -332,13 +388,21 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
         smem_set = smem;
     }
     const int64_t items = T * g.nchunk;
-    if (items >= ((int64_t)1 << 31))
+    if (items >= ((int64_t)1 << 30))
         return EP_ERR_UNSUPPORTED;
-    const int grid = (int)std::min<int64_t>(items, sm_count());
+    const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), sm_count());
     if (grid == 0)
         return EP_OK;
+    unsigned int *counter = nullptr;
+    if (ws != nullptr && ws_bytes >= EP_COMBINE_WS_BYTES) {
+        counter = static_cast<unsigned int *>(ws);
+        if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+    }
     gather_tma_kernel<Rows, WEIGHTED, OUT_F32><<<grid, kGatherThreads, smem, stream>>>(
-        static_cast<const uint8_t *>(y), T, g, rows, n_rows, err_bits, out, err);
+        static_cast<const uint8_t *>(y), T, g, rows, n_rows, err_bits, out, counter, err);
     return launch_status();
 }
 
@@ -353,7 +417,8 @@ static bool row_shape_ok(int64_t T, int H)
 using namespace ep;
 
 extern "C" int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
-                          int64_t num_send, void *out, int out_dtype, int32_t *err, ep_stream_t stream_)
+                          int64_t num_send, void *out, int out_dtype, void *ws, size_t ws_bytes, int32_t *err,
+                          ep_stream_t stream_)
 {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (!row_shape_ok(T, H) || P < 1 || P > EP_MAX_RANKS || num_send < 0 || num_send >= ((int64_t)1 << 31))
@@ -368,15 +433,16 @@ extern "C" int ep_combine(const void *y, int64_t T, int H, const int32_t *token_
         return EP_OK;
     const SendRows rows{token_pos, P};
     if (out_dtype == 1)
-        return launch_gather_tma<SendRows, false, true>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err,
-                                                        stream);
-    return launch_gather_tma<SendRows, false, false>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, err,
-                                                     stream);
+        return launch_gather_tma<SendRows, false, true>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, ws,
+                                                        ws_bytes, err, stream);
+    return launch_gather_tma<SendRows, false, false>(y, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, out, ws,
+                                                     ws_bytes, err, stream);
 }
 
 extern "C" int ep_batched_combine(const void *y, const int64_t *topk_idx, const float *topk_weights,
                                   const int32_t *slot, int64_t T, int K, int H, int E_local, int rank,
-                                  int max_num_tokens, void *out, int32_t *err, ep_stream_t stream_)
+                                  int max_num_tokens, void *out, void *ws, size_t ws_bytes, int32_t *err,
+                                  ep_stream_t stream_)
 {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || rank < 0 || max_num_tokens < 0)
@@ -392,5 +458,5 @@ extern "C" int ep_batched_combine(const void *y, const int64_t *topk_idx, const 
         return EP_OK;
     const BatchedRows rows{topk_idx, slot, topk_weights, K, (int64_t)rank * E_local, E_local, max_num_tokens, false};
     return launch_gather_tma<BatchedRows, true, false>(y, T, H, rows, (int64_t)E_local * max_num_tokens,
-                                                       EP_ERR_CAPACITY, out, err, stream);
+                                                       EP_ERR_CAPACITY, out, ws, ws_bytes, err, stream);
 }

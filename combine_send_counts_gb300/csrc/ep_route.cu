@@ -253,6 +253,37 @@ __device__ __forceinline__ int nth_set_bit(unsigned m, int r)
     return pos;
 }
 
+// s_tot[p] += sum over all blocks of part[bb*P + p]; s_before[p] += the same
+// over blocks bb < b.  Thread i sums rank i % P over every (blockDim/P)-th
+// block, eight loads in flight at a time, then adds into shared memory.
+// The caller zeroes s_tot / s_before and synchronises before and after.
+__device__ __forceinline__ void block_rank_sums(const int32_t *__restrict__ part, int nb, int P, int b,
+                                                int32_t *s_tot, int32_t *s_before)
+{
+    const int nsl = blockDim.x / P;
+    const int p = threadIdx.x % P, sl = threadIdx.x / P;
+    if (sl >= nsl)
+        return;
+    int tot = 0, bef = 0;
+    for (int bb0 = sl; bb0 < nb; bb0 += nsl * 8) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int bb = bb0 + u * nsl;
+            v[u] = bb < nb ? part[(int64_t)bb * P + p] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            tot += v[u];
+            bef += (bb0 + u * nsl < b) ? v[u] : 0;
+        }
+    }
+    if (tot != 0)
+        atomicAdd(&s_tot[p], tot);
+    if (bef != 0)
+        atomicAdd(&s_before[p], bef);
+}
+
 // Outputs and mode of layout_write_kernel.
 struct LayoutArgs {
     const int64_t *idx;
@@ -294,13 +325,7 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
         s_before[threadIdx.x] = 0;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < a.nb * P; i += blockDim.x) {
-        const int v = a.part_rank[i];
-        const int bb = i / P, p = i % P;
-        atomicAdd(&s_tot[p], v);
-        if (bb < b)
-            atomicAdd(&s_before[p], v);
-    }
+    block_rank_sums(a.part_rank, a.nb, P, b, s_tot, s_before);
     __syncthreads();
     if (warp == 0) {
         const int v0 = lane < P ? s_tot[lane] : 0;
@@ -662,7 +687,6 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
             else if (e != -1)
                 bad = EP_ERR_INVALID_EXPERT;
             dr[k] = (int8_t)d;
-            a.dest[t * K + k] = d;
             if (d >= 0) {
                 mask |= 1ull << d;
                 if (want_tpe) {
@@ -674,16 +698,6 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
                         atomicAdd(&s_hist[e], 1);
                 }
             }
-        }
-        uint8_t *irow = a.is_in_rank + t * P;
-        if ((P & 3) == 0) {
-            for (int p = 0; p < P; p += 4)
-                *reinterpret_cast<uint32_t *>(irow + p) =
-                    (uint32_t)((mask >> p) & 1ull) | (uint32_t)((mask >> (p + 1)) & 1ull) << 8 |
-                    (uint32_t)((mask >> (p + 2)) & 1ull) << 16 | (uint32_t)((mask >> (p + 3)) & 1ull) << 24;
-        } else {
-            for (int p = 0; p < P; ++p)
-                irow[p] = (uint8_t)((mask >> p) & 1ull);
         }
     }
     for (int p = 0; p < P; ++p) {
@@ -708,6 +722,24 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
     if (threadIdx.x == 0) {
         __threadfence();
         st_release_u64(&a.flags[b], a.tag);
+    }
+    // dest and is_in_rank are not read by other blocks: store them while the
+    // other blocks arrive
+    if (valid) {
+#pragma unroll
+        for (int k = 0; k < KM; ++k)
+            if (k < K)
+                a.dest[t * K + k] = dr[k];
+        uint8_t *irow = a.is_in_rank + t * P;
+        if ((P & 3) == 0) {
+            for (int p = 0; p < P; p += 4)
+                *reinterpret_cast<uint32_t *>(irow + p) =
+                    (uint32_t)((mask >> p) & 1ull) | (uint32_t)((mask >> (p + 1)) & 1ull) << 8 |
+                    (uint32_t)((mask >> (p + 2)) & 1ull) << 16 | (uint32_t)((mask >> (p + 3)) & 1ull) << 24;
+        } else {
+            for (int p = 0; p < P; ++p)
+                irow[p] = (uint8_t)((mask >> p) & 1ull);
+        }
     }
 
     // -------------------------------------------------------- grid barrier
@@ -743,13 +775,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
         s_before[threadIdx.x] = 0;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < nb * P; i += blockDim.x) {
-        const int v = a.part_rank[i];
-        const int bb = i / P, p = i - bb * P;
-        atomicAdd(&s_tot[p], v);
-        if (bb < b)
-            atomicAdd(&s_before[p], v);
-    }
+    block_rank_sums(a.part_rank, nb, P, b, s_tot, s_before);
     __syncthreads();
     if (warp == 0) {
         const int v0 = lane < P ? s_tot[lane] : 0;

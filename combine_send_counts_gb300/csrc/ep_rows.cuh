@@ -17,6 +17,13 @@ struct SendRows {
     __host__ __device__ __forceinline__ int len() const { return P; }
     __device__ __forceinline__ int32_t row(int64_t t, int j) const { return token_pos[t * P + j]; }
     __device__ __forceinline__ float weight(int64_t, int) const { return 1.0f; }
+    // Split lookup for prefetching: load() only issues loads, decode() uses them.
+    struct Raw {
+        int32_t pos;
+    };
+    __device__ __forceinline__ Raw load(int64_t t, int j) const { return Raw{token_pos[t * P + j]}; }
+    __device__ __forceinline__ int32_t decode(const Raw &r) const { return r.pos; }
+    __device__ __forceinline__ float weight(const Raw &) const { return 1.0f; }
 };
 
 // Expert-batched layout: slot k of token t names local expert e_l and slot s:
@@ -49,6 +56,26 @@ struct BatchedRows {
         return (int32_t)(el * M + s);
     }
     __device__ __forceinline__ float weight(int64_t t, int j) const { return w ? w[t * K + j] : 1.0f; }
+    // Split lookup for prefetching (no dedup: the combine keeps every slot).
+    struct Raw {
+        int32_t s;
+        int64_t id;
+        float w;
+    };
+    __device__ __forceinline__ Raw load(int64_t t, int j) const
+    {
+        return Raw{slot[t * K + j], idx[t * K + j], w ? w[t * K + j] : 1.0f};
+    }
+    __device__ __forceinline__ int32_t decode(const Raw &r) const
+    {
+        const int64_t el = r.id - e0;
+        if (r.s < 0 || el < 0 || el >= E_local)
+            return -1;
+        if (r.s >= M)
+            return INT32_MAX;
+        return (int32_t)(el * M + r.s);
+    }
+    __device__ __forceinline__ float weight(const Raw &r) const { return r.w; }
 };
 
 }  // namespace ep

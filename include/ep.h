@@ -62,6 +62,7 @@ enum ep_status {
 #define EP_MAX_RANKS 64
 #define EP_MAX_EXPERTS 8192
 #define EP_MAX_CHUNKS 64
+#define EP_COMBINE_WS_BYTES 16   /* optional scratch of ep_combine / ep_batched_combine */
 
 /* Human-readable name of a status value (a single bit, or EP_OK). */
 const char *ep_status_str(int status);
@@ -166,9 +167,16 @@ int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P
  * accumulated in fp32 from +0.0f and rounded once; tokens sent nowhere give
  * +0 ([AX] dispatch: unrouted tokens combine to zero).
  *   y [num_send,H] bf16.  out [T,H]: bf16 (out_dtype 0) or fp32 (out_dtype 1).
+ *   ws: optional device scratch of at least EP_COMBINE_WS_BYTES bytes (any
+ *     contents; 16-byte aligned), or NULL.  With it the SMs take work from a
+ *     shared counter that the call first clears with one cudaMemsetAsync, which
+ *     balances skewed source counts; with NULL the work is dealt round-robin.
+ *     Results are identical either way.  Calls that overlap on the GPU must not
+ *     share a ws.
  * Device errors: EP_ERR_COUNT_MISMATCH (a token_pos entry >= num_send). */
 int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
-               int64_t num_send, void *out, int out_dtype, int32_t *err, ep_stream_t stream);
+               int64_t num_send, void *out, int out_dtype, void *ws, size_t ws_bytes,
+               int32_t *err, ep_stream_t stream);
 
 /* [VB] BatchedPrepareAndFinalize.prepare, unquantised branch: the
  * expert-batched layout [E_local, max_num_tokens, H].  Local experts are
@@ -196,10 +204,12 @@ int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K,
  * with fp32 fused multiply-add from +0.0f, rounded once to bf16; tokens with
  * no local expert give +0.  Padding rows of y are never read.
  *   y [E_local, max_num_tokens, H] bf16, out [T,H] bf16.
+ *   ws: optional scratch as for ep_combine.
  * Device errors: EP_ERR_CAPACITY (a slot >= max_num_tokens). */
 int ep_batched_combine(const void *y, const int64_t *topk_idx, const float *topk_weights,
                        const int32_t *slot, int64_t T, int K, int H, int E_local, int rank,
-                       int max_num_tokens, void *out, int32_t *err, ep_stream_t stream);
+                       int max_num_tokens, void *out, void *ws, size_t ws_bytes,
+                       int32_t *err, ep_stream_t stream);
 
 /* Synthetic local expert kernel for fp8 dispatch workloads (the local_kernel
  * argument of [AX] dispatch_chunked_forward; the local kernel "weights and

@@ -62,9 +62,9 @@ def test_argument_checks_reject_before_launch(lib):
     assert lib.ep_dispatch(None, 4, 64, None, 0, 4, None, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # P = 0
     assert lib.ep_dispatch(None, 0, 64, None, 2, 0, None, None, 0, None, None) == ep.EP_OK  # empty: nothing to do
     lib.ep_combine.argtypes = [vp, ctypes.c_int64, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int64, vp,
-                               ctypes.c_int, vp, vp]
-    assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 2, None, None) == ep.EP_ERR_UNSUPPORTED  # out_dtype
-    assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # null out
+                               ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
+    assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 2, None, 0, None, None) == ep.EP_ERR_UNSUPPORTED  # dtype
+    assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 0, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # out
 
 
 def test_no_entry_point_host_code_calls_exit(lib):

@@ -432,3 +432,23 @@ def test_route_nosync_repeated_calls_reuse_workspace():
     for k in ("send_token_idx", "send_rank", "send_idx", "send_w"):   # rows past N are not written
         assert torch.equal(first[k][:N], third[k][:N]), k
     assert int(first["err"].item()) == int(second["err"].item()) == int(third["err"].item()) == 0
+
+
+@pytest.mark.parametrize("name", ["mid", "large"])
+def test_combine_static_and_shared_work_split_agree(name):
+    # The combine deals (token, chunk) items to the SMs either round-robin (no
+    # scratch) or from a shared counter (with scratch); the results are the
+    # same bits and equal the oracle.
+    w = wl.WORKLOADS[name]
+    idx, wts = wl.routing(w)
+    o = oracle.compute_send_counts(idx, w.P, w.E_local, with_tokens_per_expert=False)
+    ol = oracle.build_send_layout(idx, wts, o["dest"], o["is_in_rank"], w.E_local)
+    y = wl.expert_outputs(w, ol["n"])
+    want = oracle.combine(y, ol["token_pos"])
+    yd, tp = y.cuda(), torch.from_numpy(ol["token_pos"]).cuda()
+    a = ep.combine_rows(yd, tp, ws=None)
+    b = ep.combine_rows(yd, tp)
+    c = ep.combine_rows(yd, tp, ws=ep.combine_ws())
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(b, c)
+    assert_combine_parity("combine", bits16(b), want)
