@@ -69,9 +69,21 @@ _SIGNATURES = {
     "ep_local_expert_fp8": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP]),
     "ep_route_nosync": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "ep_local_expert_fp8_callback": (_I32, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ep_compute_send_counts_noalloc": (_I32, [_VP, _I64, _I32, _I32, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
                                               _VP, _VP]),
 }
+
+
+class EPChunkBuffers(ctypes.Structure):
+    """ep_chunk_buffers of include/ep.h."""
+    _fields_ = [("dest", _VP), ("is_in_rank", _VP), ("send_counts", _VP), ("rank_offsets", _VP),
+                ("token_pos", _VP), ("max_rows", _I64), ("send_token_idx", _VP), ("send_rank", _VP),
+                ("send_idx", _VP), ("send_w", _VP), ("recv_x", _VP), ("recv_scale", _VP), ("local_out", _VP),
+                ("ws", _VP), ("ws_bytes", _SZ), ("combine_ws", _VP)]
+
+
+LOCAL_KERNEL_FN = ctypes.CFUNCTYPE(_I32, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP)
 
 
 def library_path() -> str:
@@ -93,6 +105,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    lib.ep_dispatch_chunked_forward.restype = _I32
+    lib.ep_dispatch_chunked_forward.argtypes = [_VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32,
+                                                LOCAL_KERNEL_FN, _VP, _VP, ctypes.POINTER(EPChunkBuffers), _VP,
+                                                _VP, _VP]
     _lib = lib
     return lib
 
@@ -215,6 +231,22 @@ def ep_compute_send_counts_noalloc(topk_idx, T, K, P, E_local, h_chunk_bounds, c
                                                int(chunks), _p(dest), _p(is_in_rank), _p(send_counts),
                                                _p(rank_offsets), _p(tokens_per_expert), _p(err), _stream(stream))
     _check(rc, "ep_compute_send_counts_noalloc")
+
+
+def ep_dispatch_chunked_forward(x, topk_idx, topk_weights, T, K, H, P, E_local, chunks, fp8, local_kernel, user,
+                                out, buffers: EPChunkBuffers, h_counts, err, stream=None):
+    """local_kernel: a LOCAL_KERNEL_FN (ctypes callback or the library's
+    ep_local_expert_fp8_callback); h_counts: pinned host int32 [chunks*P]."""
+    rc = load().ep_dispatch_chunked_forward(_p(x), _p(topk_idx), _p(topk_weights), int(T), int(K), int(H), int(P),
+                                            int(E_local), int(chunks), int(fp8), local_kernel, user, _p(out),
+                                            ctypes.byref(buffers), ctypes.c_void_p(h_counts.data_ptr()), _p(err),
+                                            _stream(stream))
+    _check(rc, "ep_dispatch_chunked_forward")
+
+
+def ep_local_expert_fp8_callback():
+    """The library's synthetic fp8 expert as a LOCAL_KERNEL_FN."""
+    return LOCAL_KERNEL_FN(ctypes.cast(load().ep_local_expert_fp8_callback, ctypes.c_void_p).value)
 
 
 # ------------------------------------------------------------------ helpers --
@@ -402,4 +434,66 @@ def local_expert_fp8(recv_q, recv_scale, send_idx, send_w, err=None, stream=None
     out = torch.empty((N, H), dtype=torch.bfloat16, device=recv_q.device)
     err = err if err is not None else error_word(recv_q.device)
     ep_local_expert_fp8(recv_q, recv_scale, send_idx, send_w, N, K, H, out, err, stream)
+    return out
+
+
+def dispatch_chunked_forward(x, topk_idx, topk_weights, *, num_local_experts: int, num_ranks: int, chunks: int,
+                             fp8: bool = False, local_kernel=None, err=None, stream=None):
+    """The axolotl dispatch_chunked_forward on one GPU through the native driver.
+
+    local_kernel: None for the library's synthetic fp8 expert (fp8 only), or a
+    Python callable f(chunk, recv_x, recv_scale, send_idx, send_w, local_out)
+    receiving torch views of the chunk's n rows, which must fill local_out
+    (bf16 [n, H]) with the weighted sum over K of its experts on the current
+    stream.  Returns out [T,H] bf16."""
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    P, El = num_ranks, num_local_experts
+    dev = x.device
+    bounds = chunk_bounds(T, chunks)
+    max_len = max(bounds[i + 1] - bounds[i] for i in range(chunks))
+    R = max(max_len * min(K, P), 1)
+    t = dict(
+        dest=torch.empty((T, K), dtype=torch.int32, device=dev),
+        is_in_rank=torch.empty((T, P), dtype=torch.uint8, device=dev),
+        send_counts=torch.empty((chunks, P), dtype=torch.int32, device=dev),
+        rank_offsets=torch.empty((chunks, P + 1), dtype=torch.int32, device=dev),
+        token_pos=torch.empty((T, P), dtype=torch.int32, device=dev),
+        send_token_idx=torch.empty(R, dtype=torch.int32, device=dev),
+        send_rank=torch.empty(R, dtype=torch.int32, device=dev),
+        send_idx=torch.empty((R, K), dtype=torch.int64, device=dev),
+        send_w=torch.empty((R, K), dtype=torch.float32, device=dev),
+        recv_x=torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev),
+        recv_scale=torch.empty((R, H // 128), dtype=torch.float32, device=dev) if fp8 else None,
+        local_out=torch.empty((R, H), dtype=torch.bfloat16, device=dev),
+        ws=workspace(T, K, P, El, chunks, dev),
+        combine_ws=combine_ws(dev),
+    )
+    b = EPChunkBuffers()
+    for f, _ in EPChunkBuffers._fields_:
+        if f == "max_rows":
+            b.max_rows = R
+        elif f == "ws_bytes":
+            b.ws_bytes = t["ws"].numel()
+        else:
+            v = t[f]
+            setattr(b, f, None if v is None else v.data_ptr())
+    h_counts = torch.empty(chunks * P, dtype=torch.int32, pin_memory=True)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    err = err if err is not None else error_word(dev)
+    if local_kernel is None:
+        if not fp8:
+            raise ValueError("the built-in local kernel is the fp8 synthetic expert")
+        cb = ep_local_expert_fp8_callback()
+    else:
+        def _py_kernel(user, chunk, n, K_, H_, rx, rs, si, sw, lo, err_p, stream_p):
+            try:
+                local_kernel(chunk, t["recv_x"][:n], None if t["recv_scale"] is None else t["recv_scale"][:n],
+                             t["send_idx"][:n], t["send_w"][:n], t["local_out"][:n])
+                return EP_OK
+            except Exception:  # reported to the driver as a failed step
+                return EP_ERR_INVALID_ARG
+        cb = LOCAL_KERNEL_FN(_py_kernel)
+    ep_dispatch_chunked_forward(x, topk_idx, topk_weights, T, K, H, P, El, chunks, int(fp8), cb, None, out, b,
+                                h_counts, err, stream)
     return out

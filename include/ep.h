@@ -223,6 +223,59 @@ int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const in
                         const float *send_w, int64_t N, int K, int H, void *out,
                         int32_t *err, ep_stream_t stream);
 
+/* [AX] dispatch_chunked_forward on one GPU: dispatch -> local_kernel ->
+ * combine over `chunks` contiguous token ranges ([AX] chunk_bounds).  The
+ * split counts of every chunk come from ONE ep_compute_send_counts launch and
+ * ONE device-to-host copy (into h_counts, pinned host memory of chunks*P
+ * int32, after which the host waits once); then, per chunk in order on
+ * `stream`: ep_build_send_layout, ep_dispatch (bf16, or fp8 when fp8 = 1),
+ * local_kernel, ep_combine into the chunk's rows of out [T,H] bf16.  The
+ * pages overlap the next chunk's all-to-alls with the current chunk's expert
+ * compute; one GPU has no exchange to hide, so chunks run in order.
+ *   local_kernel: called once per chunk with the chunk's received rows
+ *     (recv_x, recv_scale, send_idx, send_w, n_rows of them) and must enqueue,
+ *     on `stream`, the weighted sum over K of its experts into local_out
+ *     [n_rows, H] bf16 ([AX] module description); it returns an ep_status.
+ *     ep_local_expert_fp8_callback is the synthetic fp8 expert as a callback.
+ *   b: device buffers sized by the caller; every chunk's rows must fit in
+ *     max_rows (else EP_ERR_CAPACITY, returned before that chunk runs).
+ * Returns the first non-OK status of the calls it makes. */
+typedef int (*ep_local_kernel_fn)(void *user, int chunk, int64_t n_rows, int K, int H,
+                                  const void *recv_x, const float *recv_scale,
+                                  const int64_t *send_idx, const float *send_w, void *local_out,
+                                  int32_t *err, ep_stream_t stream);
+
+typedef struct ep_chunk_buffers {
+    int32_t *dest;             /* [T,K] */
+    uint8_t *is_in_rank;       /* [T,P] */
+    int32_t *send_counts;      /* [chunks,P] */
+    int32_t *rank_offsets;     /* [chunks,P+1] */
+    int32_t *token_pos;        /* [T,P] */
+    int64_t max_rows;          /* rows of the per-chunk buffers below */
+    int32_t *send_token_idx;   /* [max_rows] */
+    int32_t *send_rank;        /* [max_rows] */
+    int64_t *send_idx;         /* [max_rows,K] */
+    float *send_w;             /* [max_rows,K] */
+    void *recv_x;              /* [max_rows,H] bf16, or e4m3 when fp8 */
+    float *recv_scale;         /* [max_rows,H/128] when fp8, else NULL */
+    void *local_out;           /* [max_rows,H] bf16 */
+    void *ws;                  /* ep_workspace_size(T, K, P, E_local, chunks) bytes */
+    size_t ws_bytes;
+    void *combine_ws;          /* EP_COMBINE_WS_BYTES bytes, or NULL */
+} ep_chunk_buffers;
+
+int ep_dispatch_chunked_forward(const void *x, const int64_t *topk_idx, const float *topk_weights,
+                                int64_t T, int K, int H, int P, int E_local, int chunks, int fp8,
+                                ep_local_kernel_fn local_kernel, void *user, void *out,
+                                const ep_chunk_buffers *b, int32_t *h_counts, int32_t *err,
+                                ep_stream_t stream);
+
+/* ep_local_expert_fp8 in the ep_local_kernel_fn shape (user and chunk unused). */
+int ep_local_expert_fp8_callback(void *user, int chunk, int64_t n_rows, int K, int H,
+                                 const void *recv_x, const float *recv_scale,
+                                 const int64_t *send_idx, const float *send_w, void *local_out,
+                                 int32_t *err, ep_stream_t stream);
+
 /* Same as ep_compute_send_counts, but the caller passes no workspace: the
  * scratch lives in one fixed device array of EP_NOALLOC_SCRATCH_BYTES that the
  * library holds on every device that loads it, until the process exits.  The
