@@ -29,6 +29,10 @@ __device__ __forceinline__ unsigned lanemask_lt()
 }
 
 // 16-byte streaming load that bypasses L1 (every row byte is used once).
+// Volatile on purpose: callers guard it with a bounds test, and a non-volatile
+// asm may be speculated out of that guard (a load past the end of a buffer).
+// Callers that want many loads in flight issue them in a loop of their own
+// before using the values.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 {
     uint4 v;

@@ -126,13 +126,17 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
     for (int base = 0; base < g.nvec; base += g.G * U) {
         uint2 q[U];
         float scale[U];
+        uint4 vin[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {            // all loads first: U vectors in flight
+            const int i = base + lt + u * g.G;
+            vin[u] = make_uint4(0, 0, 0, 0);
+            if (i < g.nvec)
+                vin[u] = ld_stream(src + i);
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int i = base + lt + u * g.G;
-            const bool ok = i < g.nvec;            // uniform over each half-warp
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (ok)
-                v = ld_stream(src + i);
+            const uint4 v = vin[u];                // invalid vectors are whole half-warps of zeros
             float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
             float amax = 0.0f;
