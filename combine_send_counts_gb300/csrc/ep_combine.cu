@@ -203,20 +203,29 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
                 ++k;
                 const int col0 = chunk * g.CH;
                 const uint32_t bytes = (uint32_t)min(g.CH, g.H - col0) * 2u;
+                // Sources are issued in rounds of B ordinals: within a round
+                // every buffer appears once, and a lane waits on a buffer only
+                // after the buffer's previous use has been armed (an earlier
+                // round or item).  Waiting earlier could match a parity two
+                // phases back and re-arm a buffer still in use.
+                for (int round = 0; (round << g.logB) < nsrc; ++round) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int32_t r = h == 0 ? r0 : r1;
-                    if (!mine || r < 0)
-                        continue;
-                    const uint32_t u = use + (h == 0 ? o0 : o1);
-                    const int b = (int)(u & (g.B - 1));
-                    if (u >= (uint32_t)g.B && !mbar_wait(&empty[b], ((u >> g.logB) - 1) & 1, kWaitNs)) {
-                        ok = false;
-                        continue;
+                    for (int h = 0; h < 2; ++h) {
+                        const int32_t r = h == 0 ? r0 : r1;
+                        const int o = h == 0 ? o0 : o1;
+                        if (!mine || r < 0 || (o >> g.logB) != round)
+                            continue;
+                        const uint32_t u = use + o;
+                        const int b = (int)(u & (g.B - 1));
+                        if (u >= (uint32_t)g.B && !mbar_wait(&empty[b], ((u >> g.logB) - 1) & 1, kWaitNs)) {
+                            ok = false;
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(&full[b], bytes);
+                        bulk_g2s(ring + (size_t)b * g.RB, y + ((int64_t)r * g.H + col0) * 2, bytes, &full[b]);
+                        last_use[b] = u;
                     }
-                    mbar_arrive_expect_tx(&full[b], bytes);
-                    bulk_g2s(ring + (size_t)b * g.RB, y + ((int64_t)r * g.H + col0) * 2, bytes, &full[b]);
-                    last_use[b] = u;
+                    __syncwarp();
                 }
                 use += nsrc;
                 ok = __all_sync(kFull, ok);

@@ -510,3 +510,36 @@ def test_chunked_driver_fp8_full_size_sampled():
         q, sc = oracle.dispatch_fp8(x[t:t + 1], lay["send_token_idx"])
         want = oracle.combine(oracle.local_expert_fp8(q, sc, lay["send_idx"], lay["send_w"]), lay["token_pos"])
         assert_combine_parity(f"token {t}", outb[t:t + 1], want)
+
+
+# ----------------------------------------- items with more sources than buffers --
+# With H = 7168 the combine's shared-memory ring holds 8 rows; these cases give
+# every token 16 or 32 source rows, so each item reuses ring buffers within
+# itself (the producer must issue it in rounds).
+@pytest.mark.parametrize("T,K,P", [(600, 16, 16), (300, 32, 32)])
+def test_combine_items_longer_than_the_ring(T, K, P):
+    H, E_local = 7168, 1
+    idx, wts = _routing(T, K, P * E_local, seed=T + K, frac_unrouted=0.0)
+    x = _randn(T, H, 5)
+    o = oracle.send_path(x, idx, wts, None, P, E_local)
+    assert int((o["layout"]["token_pos"] >= 0).sum(1).min()) == P      # every token hits every rank
+    y = _randn(o["layout"]["n"], H, 6)
+    o["out"] = oracle.combine(y, o["layout"]["token_pos"])
+    g = gpu_send_path(x, idx, wts, y, P, E_local)
+    compare_send_path(x, idx, wts, y, P, E_local, g, o)
+
+
+def test_batched_combine_items_longer_than_the_ring():
+    T, H, K, E, E_local, rank, M = 300, 7168, 32, 32, 32, 0, 400
+    idx, wts = _routing(T, K, E, seed=77, frac_unrouted=0.0)           # all 32 experts local
+    x = _randn(T, H, 7)
+    o = oracle.batched_prepare(x, idx, E, E_local, rank, M)
+    w = wl.Workload("long", T=T, H=H, E=E, K=K, P=1, routing="uniform", rank=rank, max_num_tokens=M)
+    y = wl.batched_expert_outputs(w, o["tokens_per_expert"])
+    want = oracle.batched_combine(y, idx, wts, o["slot"], E_local, rank)
+    dev = "cuda"
+    r = ep.batched_prepare(x.to(dev), idx.to(dev), E, E_local, rank, M)
+    got = ep.batched_combine(y.to(dev), idx.to(dev), wts.to(dev), r["slot"], rank, err=r["err"])
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    assert_combine_parity("batched combine", bits16(got), want)
