@@ -40,6 +40,6 @@ struct ChunkTable {
 // Launchers implemented in ep_route.cu and used by the batched entry points.
 int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
                          int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
-                         int32_t *part, int32_t *err, cudaStream_t stream);
+                         void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream);
 
 }  // namespace ep

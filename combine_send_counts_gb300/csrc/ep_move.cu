@@ -373,7 +373,7 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
         return EP_ERR_INVALID_ARG;
 
     int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, max_num_tokens, tokens_per_expert,
-                                  slot, static_cast<int32_t *>(ws), err, stream);
+                                  slot, ws, ws_bytes, err, stream);
     if (rc != EP_OK)
         return rc;
     if (T > 0) {

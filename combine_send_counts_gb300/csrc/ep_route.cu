@@ -571,27 +571,6 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
     raise(err, bad);
 }
 
-int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
-                         int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
-                         int32_t *part, int32_t *err, cudaStream_t stream)
-{
-    const int nb = (int)ceil_div(T, kRouteThreads);
-    const int64_t e0 = (int64_t)rank * E_local;
-    if (nb > 0) {
-        batched_count_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E, E_local, e0, part, err);
-        if (launch_status() != EP_OK)
-            return EP_ERR_CUDA;
-        batched_slot_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E_local, e0, max_num_tokens,
-                                                              part, nb, tokens_per_expert, slot, err);
-        return launch_status();
-    }
-    // T == 0: every expert receives nothing.
-    if (cudaMemsetAsync(tokens_per_expert, 0, sizeof(int32_t) * E_local, stream) != cudaSuccess)
-        return EP_ERR_CUDA;
-    return EP_OK;
-}
-
-
 // ------------------------------------------------------- fused route kernel --
 // Counts and send layout in one cooperative launch (all blocks resident at
 // once).  Each thread owns one token and keeps its K expert ids, weights and
@@ -908,6 +887,214 @@ static unsigned long long next_route_tag()
         v = epoch.fetch_add(0x632be59bd9b4e019ull);
     } while (v == 0);
     return v;
+}
+
+// ------------------------------------------------ fused expert-batched slots --
+// The slots of the expert-batched layout in one cooperative launch, like the
+// fused route: each thread keeps its token's K expert ids in registers, warp
+// ballots per local expert give block counts, every block publishes them with
+// a tagged arrival flag, and after the bounded grid barrier each thread takes
+// its slot from the block bases and its ballot prefix.  Needs E_local <= 64.
+struct BatchedFusedArgs {
+    const int64_t *idx;
+    int64_t T;
+    int K, E, E_local;
+    int64_t e0;
+    int M;
+    int32_t *tokens_per_expert;
+    int32_t *slot;
+    int32_t *part;                    // [gridDim][E_local]
+    unsigned long long *flags;        // [gridDim]
+    unsigned long long tag;
+    int32_t *err;
+};
+
+template <int KC>
+__global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFusedArgs a)
+{
+    constexpr int KM = KC > 0 ? KC : EP_MAX_TOPK;
+    __shared__ int32_t s_warp[kFusedWarps][64];
+    __shared__ int32_t s_tot[64], s_before[64];
+    __shared__ int s_fail;
+    const int K = KC > 0 ? KC : a.K;
+    const int El = a.E_local;
+    const int b = blockIdx.x, nb = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)b * kFusedThreads + threadIdx.x;
+    const bool valid = t < a.T;
+    if (threadIdx.x == 0)
+        s_fail = 0;
+
+    int64_t id[KM];
+    uint64_t mask = 0;
+    int bad = 0;
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+        id[k] = -1;
+        if (valid && k < K)
+            id[k] = a.idx[t * K + k];
+    }
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+        if (!valid || k >= K)
+            continue;
+        if (id[k] < -1 || id[k] >= a.E)
+            bad = EP_ERR_INVALID_EXPERT;
+        const int64_t el = id[k] - a.e0;
+        if (el >= 0 && el < El)
+            mask |= 1ull << el;
+    }
+    for (int e = 0; e < El; ++e) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
+        if (lane == 0)
+            s_warp[warp][e] = __popc(bal);
+    }
+    __syncthreads();
+    if (threadIdx.x < El) {
+        int run = 0;
+        for (int ww = 0; ww < kFusedWarps; ++ww) {
+            const int v = s_warp[ww][threadIdx.x];
+            s_warp[ww][threadIdx.x] = run;
+            run += v;
+        }
+        a.part[(int64_t)b * El + threadIdx.x] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        st_release_u64(&a.flags[b], a.tag);
+    }
+    {
+        bool ok = true;
+        for (int i = threadIdx.x; i < nb && ok; i += blockDim.x) {
+            if (ld_acquire_u64(&a.flags[i]) == a.tag)
+                continue;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_u64(&a.flags[i]) != a.tag)
+                if (global_timer_ns() - t0 > kBarrierNs) {
+                    ok = false;
+                    break;
+                }
+        }
+        if (!ok)
+            s_fail = 1;
+        __threadfence();
+        __syncthreads();
+        if (s_fail) {
+            if (threadIdx.x == 0)
+                raise(a.err, EP_ERR_TIMEOUT);
+            return;
+        }
+    }
+    if (threadIdx.x < El) {
+        s_tot[threadIdx.x] = 0;
+        s_before[threadIdx.x] = 0;
+    }
+    __syncthreads();
+    block_rank_sums(a.part, nb, El, b, s_tot, s_before);
+    __syncthreads();
+    if (b == 0 && threadIdx.x < El) {
+        const int tot = s_tot[threadIdx.x];
+        a.tokens_per_expert[threadIdx.x] = min(tot, a.M);
+        if (tot > a.M)
+            bad = EP_ERR_CAPACITY;
+    }
+    int32_t sl[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+        sl[k] = -1;
+    for (int e = 0; e < El; ++e) {
+        const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
+        if (!((mask >> e) & 1ull))
+            continue;
+        const int s = s_before[e] + s_warp[warp][e] + __popc(bal & lanemask_lt());
+        const int v = s < a.M ? s : -1;
+        if (s >= a.M)
+            bad = EP_ERR_CAPACITY;
+#pragma unroll
+        for (int k = 0; k < KM; ++k)
+            if (k < K && id[k] == a.e0 + e)
+                sl[k] = v;
+    }
+    if (valid) {
+#pragma unroll
+        for (int k = 0; k < KM; ++k)
+            if (k < K)
+                a.slot[t * K + k] = sl[k];
+    }
+    raise(a.err, bad);
+}
+
+template <int KC>
+static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t stream, bool *launched)
+{
+    *launched = false;
+    static int max_per_sm = -1;
+    if (max_per_sm < 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, batched_fused_kernel<KC>, kFusedThreads, 0) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        max_per_sm = n;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_OK;
+    }
+    if ((int64_t)max_per_sm * sms < nb)
+        return EP_OK;
+    BatchedFusedArgs copy = a;
+    void *args[] = {&copy};
+    if (cudaLaunchCooperativeKernel((const void *)batched_fused_kernel<KC>, dim3(nb), dim3(kFusedThreads), args, 0,
+                                    stream) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    *launched = true;
+    return EP_OK;
+}
+
+int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
+                         int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
+                         void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream)
+{
+    const int64_t e0 = (int64_t)rank * E_local;
+    if (T == 0) {   // every expert receives nothing
+        if (cudaMemsetAsync(tokens_per_expert, 0, sizeof(int32_t) * E_local, stream) != cudaSuccess)
+            return EP_ERR_CUDA;
+        return EP_OK;
+    }
+    // one cooperative launch when the local experts fit one mask word, the
+    // blocks can be resident together and the workspace holds partials + flags
+    const int nbf = (int)ceil_div(T, kFusedThreads);
+    const size_t part_bytes = align_up((size_t)nbf * E_local * sizeof(int32_t), kWsAlign);
+    if (E_local <= 64 && ws_bytes >= part_bytes + (size_t)nbf * sizeof(unsigned long long)) {
+        BatchedFusedArgs fa{topk_idx, T, K, E, E_local, e0, max_num_tokens, tokens_per_expert, slot,
+                            static_cast<int32_t *>(ws),
+                            reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + part_bytes),
+                            next_route_tag(), err};
+        bool launched = false;
+        int rc;
+        switch (K) {
+        case 2: rc = launch_batched_fused<2>(fa, nbf, stream, &launched); break;
+        case 4: rc = launch_batched_fused<4>(fa, nbf, stream, &launched); break;
+        case 6: rc = launch_batched_fused<6>(fa, nbf, stream, &launched); break;
+        case 8: rc = launch_batched_fused<8>(fa, nbf, stream, &launched); break;
+        default: rc = launch_batched_fused<0>(fa, nbf, stream, &launched); break;
+        }
+        if (rc != EP_OK || launched)
+            return rc;
+    }
+    const int nb = (int)ceil_div(T, kRouteThreads);
+    int32_t *part = static_cast<int32_t *>(ws);
+    batched_count_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E, E_local, e0, part, err);
+    if (launch_status() != EP_OK)
+        return EP_ERR_CUDA;
+    batched_slot_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E_local, e0, max_num_tokens, part, nb,
+                                                          tokens_per_expert, slot, err);
+    return launch_status();
 }
 }  // namespace ep
 

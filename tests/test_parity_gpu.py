@@ -543,3 +543,17 @@ def test_batched_combine_items_longer_than_the_ring():
     torch.cuda.synchronize()
     assert int(r["err"].item()) == 0
     assert_combine_parity("batched combine", bits16(got), want)
+
+
+def test_batched_prepare_many_local_experts():
+    # E_local = 128 > 64 takes the two-kernel slot path instead of the fused one
+    T, H, K, E, E_local, rank, M = 700, 64, 8, 256, 128, 1, 300
+    idx, wts = _routing(T, K, E, seed=31, dup=True)
+    x = _randn(T, H, 8)
+    o = oracle.batched_prepare(x, idx, E, E_local, rank, M)
+    dev = "cuda"
+    r = ep.batched_prepare(x.to(dev), idx.to(dev), E, E_local, rank, M)
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), o["tokens_per_expert"])
+    assert_equal("slot", np_(r["slot"]), o["slot"])
