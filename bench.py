@@ -428,6 +428,10 @@ def run_gpu(args):
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, y, stream, world, dist)
+    if not args.no_other_paths and not args.tokens:
+        del sp, y
+        torch.cuda.empty_cache()
+        result["other_paths"] = run_other_paths(ep, torch, wl, dev, flush, peak, iters=10)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, x_h, idx_h, w_h, y_h, args.cpu_steps, full=True)
     if world > 1:
@@ -435,6 +439,77 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def _event_time_us(torch, flush, fn, iters, warmup=2):
+    ts = []
+    for i in range(warmup + iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= warmup:
+            ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.mean(ts)
+
+
+def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
+    """The other rows of the path, each on its own workload: expert-batched
+    prepare and combine (batched workload), fp8 dispatch of one chunk and the
+    native chunked fp8 forward (chunked fp8 workload).  Routing follows each
+    workload's recipe; row values are drawn on the device (they do not change
+    the work)."""
+    out = {}
+    g = torch.Generator(device=dev).manual_seed(0)
+    err = ep.error_word(dev)
+    cws = ep.combine_ws(dev)
+
+    w = wl.WORKLOADS["batched"]
+    idx, wts = (t.to(dev) for t in wl.routing(w))
+    x = torch.randn((w.T, w.H), device=dev, generator=g).to(torch.bfloat16)
+    r = ep.batched_prepare(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, err=err)
+    hits = int(r["tokens_per_expert"].sum().item())
+    ws = ep.workspace(w.T, w.K, w.P, w.E_local, 1, dev)
+    ab = (w.T + hits) * w.H * 2
+    us = _event_time_us(torch, flush, lambda: ep.ep_batched_prepare(
+        x, idx, w.T, w.K, w.H, w.E, w.E_local, w.rank, w.max_num_tokens, r["b_x"], r["tokens_per_expert"],
+        r["slot"], 0, ws, err), iters)
+    out["batched_prepare"] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab,
+                              "gbs": round(ab / us / 1e3, 1), "frac": round(ab / us / 1e3 / peak, 4),
+                              "local_hits": hits}
+    y = torch.randn((w.E_local, w.max_num_tokens, w.H), device=dev, generator=g).to(torch.bfloat16)
+    o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    us = _event_time_us(torch, flush, lambda: ep.ep_batched_combine(
+        y, idx, wts, r["slot"], w.T, w.K, w.H, w.E_local, w.rank, w.max_num_tokens, o, cws, err), iters)
+    out["batched_combine"] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab,
+                              "gbs": round(ab / us / 1e3, 1), "frac": round(ab / us / 1e3 / peak, 4)}
+    del x, y, o, r
+
+    w = wl.WORKLOADS["chunk_fp8"]
+    idx, wts = (t.to(dev) for t in wl.routing(w))
+    x = torch.randn((w.T, w.H), device=dev, generator=g).to(torch.bfloat16)
+    Tc = w.T // w.chunks
+    rr = ep.route_nosync(idx[:Tc], wts[:Tc], w.P, w.E_local, err=err)
+    N = int(rr["rank_offsets"][w.P].item())
+    q = torch.empty((N, w.H), dtype=torch.uint8, device=dev)
+    sc = torch.empty((N, w.H // 128), dtype=torch.float32, device=dev)
+    ab = Tc * w.H * 2 + N * (w.H + w.H // 32)
+    us = _event_time_us(torch, flush, lambda: ep.ep_dispatch(x[:Tc], Tc, w.H, rr["token_pos"], w.P, N, q, sc, 1,
+                                                             err), iters)
+    out["fp8_dispatch"] = {"workload": f"chunk_fp8, one chunk of {Tc} tokens", "us": round(us, 2),
+                           "algorithmic_bytes": ab, "gbs": round(ab / us / 1e3, 1),
+                           "frac": round(ab / us / 1e3 / peak, 4), "rows": N}
+    us = _event_time_us(torch, flush, lambda: ep.dispatch_chunked_forward(
+        x, idx, wts, num_local_experts=w.E_local, num_ranks=w.P, chunks=w.chunks, fp8=True, err=err),
+        max(2, iters // 4), warmup=1)
+    out["chunked_fp8_forward"] = {"workload": "chunk_fp8 (T=32768, 4 chunks, synthetic fp8 expert included)",
+                                  "us": round(us, 1), "tokens_per_s": round(w.T / us * 1e6, 1)}
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise ep.EPError(int(err.item()), "other paths")
+    return out
 
 
 def run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, y_dev, stream, world, dist):
@@ -535,6 +610,7 @@ def main(argv=None):
                     help="run the workload's recipe with this many tokens instead (reduced cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-other-paths", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-warmup", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
