@@ -369,7 +369,7 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
         return EP_ERR_INVALID_ARG;
     if ((int64_t)E_local * max_num_tokens > 0 && (b_x == nullptr || !aligned(b_x, 16)))
         return EP_ERR_INVALID_ARG;
-    if (ws_bytes < (size_t)ceil_div(T, kRouteThreads) * E_local * sizeof(int32_t))
+    if (ws_bytes < kWsAlign + (size_t)ceil_div(T, kRouteThreads) * E_local * sizeof(int32_t))
         return EP_ERR_INVALID_ARG;
 
     int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, max_num_tokens, tokens_per_expert,

@@ -577,11 +577,77 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
 // owning ranks in registers from the counting phase to the layout phase;
 // between the two, every block publishes its per-rank partial counts and an
 // arrival flag, and waits (bounded) until every block's flag carries this
-// call's tag.  Flags from earlier calls carry older tags, so the workspace
-// needs no initialisation.
+// launch's tag.
 constexpr int kFusedThreads = 128;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr uint64_t kBarrierNs = 500000000ull;   // 0.5 s
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier of the cooperative routing kernels.  A launch's tag mixes the
+// host's per-call tag with a launch counter kept in the workspace header, so
+// that replays of one captured launch (a CUDA graph repeats the host tag)
+// still get a tag that no flag left by an earlier launch holds; the workspace
+// needs no initialisation.  Block 0 advances the counter after its wait: by
+// then every block has arrived, and a block reads the counter before it
+// arrives.
+struct GridBarrier {
+    unsigned long long *flags;    // [gridDim]
+    unsigned long long *epoch;    // launch counter (workspace header)
+    unsigned long long host_tag;  // different for every host call
+};
+
+// Thread 0 only: this launch's tag and the counter value it was made from.
+__device__ __forceinline__ unsigned long long barrier_tag(const GridBarrier &g, unsigned long long *e_out)
+{
+    const unsigned long long e = *reinterpret_cast<const volatile unsigned long long *>(g.epoch);
+    *e_out = e;
+    const unsigned long long tag = g.host_tag ^ (e * 0x9e3779b97f4a7c15ull);
+    return tag != 0 ? tag : 1;
+}
+
+// Thread 0 only, after a __syncthreads that follows every write the other
+// blocks will read.
+__device__ __forceinline__ void barrier_arrive(const GridBarrier &g, unsigned long long tag)
+{
+    __threadfence();
+    st_release_u64(&g.flags[blockIdx.x], tag);
+}
+
+// Whole block: waits (bounded) for every block's flag; false for the whole
+// block if one did not arrive in time.  *s_fail is a shared word cleared
+// before the block's first __syncthreads.
+__device__ __forceinline__ bool barrier_wait(const GridBarrier &g, unsigned long long tag, unsigned long long e, int *s_fail)
+{
+    bool ok = true;
+    for (int i = threadIdx.x; i < (int)gridDim.x && ok; i += blockDim.x) {
+        if (ld_acquire_u64(&g.flags[i]) == tag)
+            continue;
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_u64(&g.flags[i]) != tag)
+            if (global_timer_ns() - t0 > kBarrierNs) {
+                ok = false;
+                break;
+            }
+    }
+    if (!ok)
+        *s_fail = 1;
+    __threadfence();
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *reinterpret_cast<volatile unsigned long long *>(g.epoch) = e + 1;
+    return *s_fail == 0;
+}
 
 struct FusedArgs {
     const int64_t *idx;
@@ -598,22 +664,9 @@ struct FusedArgs {
     int32_t *token_pos;
     int32_t *part_rank;       // [gridDim][P]
     int32_t *part_expert;     // [gridDim][E] when tokens_per_expert is wanted
-    unsigned long long *flags;    // [gridDim]
-    unsigned long long tag;   // non-zero, different for every call
+    GridBarrier bar;
     int32_t *err;
 };
-
-__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // KC > 0: K == KC at compile time (vector row stores); KC == 0: any K <= 32.
 template <int KC>
@@ -624,6 +677,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
     __shared__ int32_t s_warp[kFusedWarps][EP_MAX_RANKS];
     __shared__ int32_t s_tot[EP_MAX_RANKS], s_before[EP_MAX_RANKS], s_base[EP_MAX_RANKS];
     __shared__ int s_fail;
+    __shared__ unsigned long long s_tag, s_epoch;
     const int K = KC > 0 ? KC : a.K;
     const int P = a.P, El = a.E_local, E = P * El;
     const int b = blockIdx.x, nb = gridDim.x;
@@ -636,8 +690,10 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
     if (want_tpe)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             s_hist[e] = 0;
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         s_fail = 0;
+        s_tag = barrier_tag(a.bar, &s_epoch);
+    }
     int64_t id[KM];
     float wt[KM];
     int8_t dr[KM];
@@ -698,10 +754,8 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             a.part_expert[(int64_t)b * E + e] = s_hist[e];
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        st_release_u64(&a.flags[b], a.tag);
-    }
+    if (threadIdx.x == 0)
+        barrier_arrive(a.bar, s_tag);
     // dest and is_in_rank are not read by other blocks: store them while the
     // other blocks arrive
     if (valid) {
@@ -722,30 +776,10 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
     }
 
     // -------------------------------------------------------- grid barrier
-    {
-        bool ok = true;
-        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-            if (ld_acquire_u64(&a.flags[i]) == a.tag)
-                continue;
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire_u64(&a.flags[i]) != a.tag) {
-                if (global_timer_ns() - t0 > kBarrierNs) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (!ok)
-                break;
-        }
-        if (!ok)
-            s_fail = 1;
-        __threadfence();
-        __syncthreads();
-        if (s_fail) {
-            if (threadIdx.x == 0)
-                raise(a.err, EP_ERR_TIMEOUT);
-            return;   // the whole block leaves together
-        }
+    if (!barrier_wait(a.bar, s_tag, s_epoch, &s_fail)) {
+        if (threadIdx.x == 0)
+            raise(a.err, EP_ERR_TIMEOUT);
+        return;   // the whole block leaves together
     }
 
     // --------------------------------------------------------- layout phase
@@ -904,8 +938,7 @@ struct BatchedFusedArgs {
     int32_t *tokens_per_expert;
     int32_t *slot;
     int32_t *part;                    // [gridDim][E_local]
-    unsigned long long *flags;        // [gridDim]
-    unsigned long long tag;
+    GridBarrier bar;
     int32_t *err;
 };
 
@@ -916,14 +949,17 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
     __shared__ int32_t s_warp[kFusedWarps][64];
     __shared__ int32_t s_tot[64], s_before[64];
     __shared__ int s_fail;
+    __shared__ unsigned long long s_tag, s_epoch;
     const int K = KC > 0 ? KC : a.K;
     const int El = a.E_local;
     const int b = blockIdx.x, nb = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = (int64_t)b * kFusedThreads + threadIdx.x;
     const bool valid = t < a.T;
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         s_fail = 0;
+        s_tag = barrier_tag(a.bar, &s_epoch);
+    }
 
     int64_t id[KM];
     uint64_t mask = 0;
@@ -960,31 +996,12 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
         a.part[(int64_t)b * El + threadIdx.x] = run;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        st_release_u64(&a.flags[b], a.tag);
-    }
-    {
-        bool ok = true;
-        for (int i = threadIdx.x; i < nb && ok; i += blockDim.x) {
-            if (ld_acquire_u64(&a.flags[i]) == a.tag)
-                continue;
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire_u64(&a.flags[i]) != a.tag)
-                if (global_timer_ns() - t0 > kBarrierNs) {
-                    ok = false;
-                    break;
-                }
-        }
-        if (!ok)
-            s_fail = 1;
-        __threadfence();
-        __syncthreads();
-        if (s_fail) {
-            if (threadIdx.x == 0)
-                raise(a.err, EP_ERR_TIMEOUT);
-            return;
-        }
+    if (threadIdx.x == 0)
+        barrier_arrive(a.bar, s_tag);
+    if (!barrier_wait(a.bar, s_tag, s_epoch, &s_fail)) {
+        if (threadIdx.x == 0)
+            raise(a.err, EP_ERR_TIMEOUT);
+        return;
     }
     if (threadIdx.x < El) {
         s_tot[threadIdx.x] = 0;
@@ -1068,13 +1085,16 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
     }
     // one cooperative launch when the local experts fit one mask word, the
     // blocks can be resident together and the workspace holds partials + flags
+    // workspace: [header: launch counter][partials][flags]
+    char *wsb = static_cast<char *>(ws);
     const int nbf = (int)ceil_div(T, kFusedThreads);
     const size_t part_bytes = align_up((size_t)nbf * E_local * sizeof(int32_t), kWsAlign);
-    if (E_local <= 64 && ws_bytes >= part_bytes + (size_t)nbf * sizeof(unsigned long long)) {
+    if (E_local <= 64 && ws_bytes >= kWsAlign + part_bytes + (size_t)nbf * sizeof(unsigned long long)) {
         BatchedFusedArgs fa{topk_idx, T, K, E, E_local, e0, max_num_tokens, tokens_per_expert, slot,
-                            static_cast<int32_t *>(ws),
-                            reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + part_bytes),
-                            next_route_tag(), err};
+                            reinterpret_cast<int32_t *>(wsb + kWsAlign),
+                            {reinterpret_cast<unsigned long long *>(wsb + kWsAlign + part_bytes),
+                             reinterpret_cast<unsigned long long *>(wsb), next_route_tag()},
+                            err};
         bool launched = false;
         int rc;
         switch (K) {
@@ -1088,7 +1108,7 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
             return rc;
     }
     const int nb = (int)ceil_div(T, kRouteThreads);
-    int32_t *part = static_cast<int32_t *>(ws);
+    int32_t *part = reinterpret_cast<int32_t *>(wsb + kWsAlign);
     batched_count_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E, E_local, e0, part, err);
     if (launch_status() != EP_OK)
         return EP_ERR_CUDA;
@@ -1102,9 +1122,11 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
 using namespace ep;
 
 // Workspace regions shared by the routing calls (sized for routing blocks of
-// 128 tokens, twice as many as the 256-token blocks most kernels use):
-// per-block rank counts, per-block expert counts, per-block arrival flags.
+// 128 tokens, twice as many as the 256-token blocks most kernels use): a
+// header holding the cooperative kernels' launch counter, per-block rank
+// counts, per-block expert counts, per-block arrival flags.
 struct WsLayout {
+    unsigned long long *epoch;   // header: launch counter of the cooperative kernels
     int32_t *part_rank;
     int32_t *part_expert;
     unsigned long long *flags;
@@ -1117,6 +1139,8 @@ static WsLayout ws_layout(void *ws, int64_t T, int chunks, int P, int E)
     const size_t nb = ws_blocks(T, chunks);
     char *base = static_cast<char *>(ws);
     WsLayout l;
+    l.epoch = reinterpret_cast<unsigned long long *>(base);
+    base += kWsAlign;
     l.part_rank = reinterpret_cast<int32_t *>(base);
     base += align_up(nb * P * sizeof(int32_t), kWsAlign);
     l.part_expert = reinterpret_cast<int32_t *>(base);
@@ -1132,7 +1156,7 @@ extern "C" size_t ep_workspace_size(int64_t T, int K, int P, int E_local, int ch
         return 0;
     const size_t nb = ws_blocks(T, chunks);
     const size_t E = (size_t)P * E_local;
-    return align_up(nb * P * sizeof(int32_t), kWsAlign) + align_up(nb * E * sizeof(int32_t), kWsAlign) +
+    return kWsAlign + align_up(nb * P * sizeof(int32_t), kWsAlign) + align_up(nb * E * sizeof(int32_t), kWsAlign) +
            align_up(nb * sizeof(unsigned long long), kWsAlign);
 }
 
@@ -1277,7 +1301,7 @@ extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weight
     const size_t smem_f = pe != nullptr ? sizeof(int32_t) * E : 0;
     FusedArgs fa{topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
                  rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos,
-                 wl.part_rank, pe, wl.flags, next_route_tag(), err};
+                 wl.part_rank, pe, {wl.flags, wl.epoch, next_route_tag()}, err};
     bool launched = false;
     int rc;
     switch (K) {

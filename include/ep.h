@@ -69,7 +69,11 @@ const char *ep_status_str(int status);
 
 /* Bytes of device workspace that every workspace-taking call below needs for
  * these sizes (chunks <= 1 means one chunk).  The workspace must start
- * 256-byte aligned; its contents need not be initialised and are scratch. */
+ * 256-byte aligned; its contents need not be initialised and are scratch,
+ * except that its first 256 bytes count the launches of the single-launch
+ * (cooperative) routing kernels: keep them between calls that share the
+ * workspace, captured or not.  Calls whose kernels overlap on the GPU must not
+ * share a workspace. */
 size_t ep_workspace_size(int64_t T, int K, int P, int E_local, int chunks);
 
 /* [AX] chunk_bounds (host only): `chunks` contiguous [start, end) token
@@ -137,8 +141,13 @@ int ep_build_send_layout(const int64_t *topk_idx, const float *topk_weights,
  *     suffices).  Rows N .. num_worst_rows-1 are left untouched; pass
  *     num_worst_rows as num_send to ep_dispatch / ep_combine.  If N exceeds it,
  *     EP_ERR_CAPACITY is set and rows past it are not written (token_pos -1).
- * Two kernel launches; ws as for ep_compute_send_counts with chunks = 1.
- * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_COUNT_MISMATCH. */
+ * One cooperative launch when its blocks fit on the GPU at once, else two
+ * launches; ws as for ep_compute_send_counts with chunks = 1.  The call may be
+ * captured in a CUDA graph: every replay recomputes all outputs from the
+ * current contents of topk_idx and topk_weights.
+ * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_COUNT_MISMATCH,
+ * EP_ERR_TIMEOUT (the single launch's blocks did not all arrive within 0.5 s;
+ * the outputs are then undefined). */
 int ep_route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
                     int E_local, int64_t num_worst_rows,
                     int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
@@ -191,7 +200,9 @@ int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
  * written) and sets EP_ERR_CAPACITY.
  *   x [T,H] bf16, topk_idx [T,K] int64, E = total experts (E % E_local == 0),
  *   tokens_per_expert [E_local] int32.
- * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY. */
+ *   ws: ep_workspace_size(T, K, E / E_local, E_local, 1) bytes, 256-byte
+ *     aligned (the slots then take one cooperative launch when E_local <= 64).
+ * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_TIMEOUT. */
 int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H,
                        int E, int E_local, int rank, int max_num_tokens,
                        void *b_x, int32_t *tokens_per_expert, int32_t *slot, int zero_pad,

@@ -19,6 +19,22 @@ def np_(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
+def routing_inputs(T, K, E, seed, frac_unrouted=0.1, dup=False):
+    """Seeded top-k ids (distinct per token, or with duplicates) with a share
+    of masked (-1) slots, and uniform weights (0 where masked)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    idx = (g.integers(0, E, size=(T, K)) if dup else np.argsort(g.random((T, E)), 1)[:, :K]).astype(np.int64)
+    idx[g.random((T, K)) < frac_unrouted] = -1
+    w = g.random((T, K)).astype(np.float32)
+    w[idx < 0] = 0
+    return torch.from_numpy(idx), torch.from_numpy(w)
+
+
+def randn_bf16(T, H, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    return torch.from_numpy(g.standard_normal((T, H), dtype=np.float32)).to(torch.bfloat16)
+
+
 def assert_equal(name, got, want):
     got = np.asarray(got)
     want = np.asarray(want)

@@ -14,6 +14,8 @@ import oracle
 from combine_send_counts_gb300 import workloads as wl
 
 from _paths import (assert_combine_parity, assert_equal, bits16, compare_send_path, gpu_send_path, np_)
+from _paths import randn_bf16 as _randn
+from _paths import routing_inputs as _routing
 
 pytestmark = pytest.mark.gpu
 
@@ -183,20 +185,6 @@ def test_fp8_codes_for_every_bf16_input():
 
 
 # ------------------------------------------------------------------ edges --
-def _routing(T, K, E, seed, frac_unrouted=0.1, dup=False):
-    g = np.random.Generator(np.random.PCG64(seed))
-    idx = (g.integers(0, E, size=(T, K)) if dup else np.argsort(g.random((T, E)), 1)[:, :K]).astype(np.int64)
-    idx[g.random((T, K)) < frac_unrouted] = -1
-    w = g.random((T, K)).astype(np.float32)
-    w[idx < 0] = 0
-    return torch.from_numpy(idx), torch.from_numpy(w)
-
-
-def _randn(T, H, seed):
-    g = np.random.Generator(np.random.PCG64(seed))
-    return torch.from_numpy(g.standard_normal((T, H), dtype=np.float32)).to(torch.bfloat16)
-
-
 EDGE = [
     # T, H, K, P, E_local, frac_unrouted, dup
     (1, 64, 2, 4, 2, 0.0, False),
