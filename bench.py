@@ -455,6 +455,20 @@ def _event_time_us(torch, flush, fn, iters, warmup=2):
     return statistics.mean(ts)
 
 
+def _graph_time_us(torch, flush, fn, iters, dev, warmup=2):
+    """Capture fn once (after one eager call) and time its replays."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    torch.cuda.synchronize()
+    return _event_time_us(torch, flush, g.replay, iters, warmup)
+
+
 def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
     """The other rows of the path, each on its own workload: expert-batched
     prepare and combine (batched workload), fp8 dispatch of one chunk and the
@@ -505,7 +519,27 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
         x, idx, wts, num_local_experts=w.E_local, num_ranks=w.P, chunks=w.chunks, fp8=True, err=err),
         max(2, iters // 4), warmup=1)
     out["chunked_fp8_forward"] = {"workload": "chunk_fp8 (T=32768, 4 chunks, synthetic fp8 expert included)",
+                                  "path": "one count pass, one D2H + host wait, then per chunk layout -> fp8 "
+                                          "dispatch -> expert -> combine",
                                   "us": round(us, 1), "tokens_per_s": round(w.T / us * 1e6, 1)}
+    # the same forward without a host round trip: one row set in order, two
+    # row sets pipelined over two streams, and the pipelined form replayed
+    # from a CUDA graph
+    o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    for n_sets in (1, 2):
+        f = ep.ChunkedForward(w.T, w.K, w.H, num_ranks=w.P, num_local_experts=w.E_local, chunks=w.chunks, fp8=True,
+                              n_sets=n_sets, device=dev)
+        us = _event_time_us(torch, flush, lambda: f(x, idx, wts, out=o, err=err), max(2, iters // 4))
+        key = "chunked_fp8_forward_nosync" + ("_pipelined" if n_sets == 2 else "")
+        out[key] = {"workload": "chunk_fp8 (T=32768, 4 chunks, synthetic fp8 expert included)",
+                    "path": f"ep_dispatch_chunked_forward_nosync, {n_sets} row set(s)",
+                    "us": round(us, 1), "tokens_per_s": round(w.T / us * 1e6, 1)}
+    us = _graph_time_us(torch, flush, lambda: f(x, idx, wts, out=o, err=err), max(2, iters // 4), dev)
+    out["chunked_fp8_forward_nosync_graph"] = {
+        "workload": "chunk_fp8 (T=32768, 4 chunks, synthetic fp8 expert included)",
+        "path": "ep_dispatch_chunked_forward_nosync, 2 row sets, replayed from a CUDA graph",
+        "us": round(us, 1), "tokens_per_s": round(w.T / us * 1e6, 1)}
+    del f
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise ep.EPError(int(err.item()), "other paths")

@@ -72,6 +72,8 @@ _SIGNATURES = {
     "ep_local_expert_fp8_callback": (_I32, [_VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ep_compute_send_counts_noalloc": (_I32, [_VP, _I64, _I32, _I32, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
                                               _VP, _VP]),
+    "ep_local_expert_fp8_dev_callback": (_I32, [_VP, _I32, _I64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                _VP]),
 }
 
 
@@ -84,6 +86,22 @@ class EPChunkBuffers(ctypes.Structure):
 
 
 LOCAL_KERNEL_FN = ctypes.CFUNCTYPE(_I32, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP)
+
+
+class EPRowSet(ctypes.Structure):
+    """ep_row_set of include/ep.h."""
+    _fields_ = [("send_token_idx", _VP), ("send_rank", _VP), ("send_idx", _VP), ("send_w", _VP),
+                ("recv_x", _VP), ("recv_scale", _VP), ("local_out", _VP)]
+
+
+class EPPipelineBuffers(ctypes.Structure):
+    """ep_pipeline_buffers of include/ep.h."""
+    _fields_ = [("dest", _VP), ("is_in_rank", _VP), ("send_counts", _VP), ("rank_offsets", _VP),
+                ("token_pos", _VP), ("max_rows", _I64), ("n_sets", _I32), ("sets", EPRowSet * 2),
+                ("ws", _VP), ("ws_bytes", _SZ), ("combine_ws", _VP)]
+
+
+LOCAL_KERNEL_DEV_FN = ctypes.CFUNCTYPE(_I32, _VP, _I32, _I64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP)
 
 
 def library_path() -> str:
@@ -109,6 +127,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.ep_dispatch_chunked_forward.argtypes = [_VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32,
                                                 LOCAL_KERNEL_FN, _VP, _VP, ctypes.POINTER(EPChunkBuffers), _VP,
                                                 _VP, _VP]
+    lib.ep_dispatch_chunked_forward_nosync.restype = _I32
+    lib.ep_dispatch_chunked_forward_nosync.argtypes = [_VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32,
+                                                       LOCAL_KERNEL_DEV_FN, _VP, _VP,
+                                                       ctypes.POINTER(EPPipelineBuffers), _VP, _VP, _VP]
     _lib = lib
     return lib
 
@@ -247,6 +269,23 @@ def ep_dispatch_chunked_forward(x, topk_idx, topk_weights, T, K, H, P, E_local, 
 def ep_local_expert_fp8_callback():
     """The library's synthetic fp8 expert as a LOCAL_KERNEL_FN."""
     return LOCAL_KERNEL_FN(ctypes.cast(load().ep_local_expert_fp8_callback, ctypes.c_void_p).value)
+
+
+def ep_dispatch_chunked_forward_nosync(x, topk_idx, topk_weights, T, K, H, P, E_local, chunks, fp8, local_kernel,
+                                       user, out, buffers: EPPipelineBuffers, err, stream=None, aux_stream=None):
+    """local_kernel: a LOCAL_KERNEL_DEV_FN (ctypes callback or the library's
+    ep_local_expert_fp8_dev_callback); aux_stream: the producer stream (two
+    row sets) or None (one set)."""
+    aux = None if aux_stream is None else _stream(aux_stream)
+    rc = load().ep_dispatch_chunked_forward_nosync(_p(x), _p(topk_idx), _p(topk_weights), int(T), int(K), int(H),
+                                                   int(P), int(E_local), int(chunks), int(fp8), local_kernel, user,
+                                                   _p(out), ctypes.byref(buffers), _p(err), _stream(stream), aux)
+    _check(rc, "ep_dispatch_chunked_forward_nosync")
+
+
+def ep_local_expert_fp8_dev_callback():
+    """The library's synthetic fp8 expert as a LOCAL_KERNEL_DEV_FN."""
+    return LOCAL_KERNEL_DEV_FN(ctypes.cast(load().ep_local_expert_fp8_dev_callback, ctypes.c_void_p).value)
 
 
 # ------------------------------------------------------------------ helpers --
@@ -496,4 +535,96 @@ def dispatch_chunked_forward(x, topk_idx, topk_weights, *, num_local_experts: in
         cb = LOCAL_KERNEL_FN(_py_kernel)
     ep_dispatch_chunked_forward(x, topk_idx, topk_weights, T, K, H, P, El, chunks, int(fp8), cb, None, out, b,
                                 h_counts, err, stream)
+    return out
+
+
+class ChunkedForward:
+    """Buffers of ep_dispatch_chunked_forward_nosync, allocated once for
+    T tokens and reused by every call (eager, or captured in a CUDA graph and
+    replayed on new contents of the same input tensors).
+
+    local_kernel: None for the library's synthetic fp8 expert (fp8 only), or a
+    Python callable f(chunk, recv_x, recv_scale, send_idx, send_w, local_out,
+    n_rows) receiving torch views of all max_rows rows of the chunk's row set
+    and n_rows, a one-element device int32 tensor with the chunk's row count;
+    it must fill local_out[:n_rows] (bf16) with the weighted sum over K of its
+    experts, enqueued on the current stream, and may write rows past n_rows.
+    n_sets: 2 pipelines chunk c+1's routing and dispatch (on an internal
+    producer stream) with chunk c's local kernel and combine; 1 runs in order."""
+
+    def __init__(self, T: int, K: int, H: int, *, num_ranks: int, num_local_experts: int, chunks: int,
+                 fp8: bool = False, n_sets: int = 2, max_rows: Optional[int] = None, local_kernel=None,
+                 device=None):
+        dev = torch.device(device or "cuda")
+        P, El = num_ranks, num_local_experts
+        bounds = chunk_bounds(T, chunks)
+        max_len = max(bounds[i + 1] - bounds[i] for i in range(chunks))
+        R = max(max_len * min(K, P), 1) if max_rows is None else int(max_rows)
+        self.T, self.K, self.H, self.P, self.El, self.chunks, self.fp8 = T, K, H, P, El, chunks, fp8
+        self.max_rows, self.n_sets = R, n_sets
+        self.t = dict(
+            dest=torch.empty((T, K), dtype=torch.int32, device=dev),
+            is_in_rank=torch.empty((T, P), dtype=torch.uint8, device=dev),
+            send_counts=torch.empty((chunks, P), dtype=torch.int32, device=dev),
+            rank_offsets=torch.empty((chunks, P + 1), dtype=torch.int32, device=dev),
+            token_pos=torch.empty((T, P), dtype=torch.int32, device=dev),
+            ws=workspace(T, K, P, El, chunks, dev),
+            combine_ws=combine_ws(dev),
+        )
+        self.sets = []
+        for _ in range(n_sets):
+            self.sets.append(dict(
+                send_token_idx=torch.empty(R, dtype=torch.int32, device=dev),
+                send_rank=torch.empty(R, dtype=torch.int32, device=dev),
+                send_idx=torch.empty((R, K), dtype=torch.int64, device=dev),
+                send_w=torch.empty((R, K), dtype=torch.float32, device=dev),
+                recv_x=torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev),
+                recv_scale=torch.empty((R, H // 128), dtype=torch.float32, device=dev) if fp8 else None,
+                local_out=torch.empty((R, H), dtype=torch.bfloat16, device=dev),
+            ))
+        b = EPPipelineBuffers()
+        for f in ("dest", "is_in_rank", "send_counts", "rank_offsets", "token_pos", "ws", "combine_ws"):
+            setattr(b, f, self.t[f].data_ptr())
+        b.max_rows, b.n_sets, b.ws_bytes = R, n_sets, self.t["ws"].numel()
+        for i, st in enumerate(self.sets):
+            for f, _ in EPRowSet._fields_:
+                setattr(b.sets[i], f, None if st[f] is None else st[f].data_ptr())
+        self.buffers = b
+        self.aux = torch.cuda.Stream(dev) if n_sets == 2 else None
+        if local_kernel is None:
+            if not fp8:
+                raise ValueError("the built-in local kernel is the fp8 synthetic expert")
+            self._cb = ep_local_expert_fp8_dev_callback()
+        else:
+            def _py_kernel(user, chunk, max_rows_, n_rows_p, K_, H_, rx, rs, si, sw, lo, err_p, stream_p):
+                try:
+                    st = self.sets[chunk % self.n_sets]
+                    n_rows = self.t["rank_offsets"][chunk, self.P:self.P + 1]
+                    local_kernel(chunk, st["recv_x"], st["recv_scale"], st["send_idx"], st["send_w"],
+                                 st["local_out"], n_rows)
+                    return EP_OK
+                except Exception:  # reported to the driver as a failed step
+                    return EP_ERR_INVALID_ARG
+            self._cb = LOCAL_KERNEL_DEV_FN(_py_kernel)
+
+    def __call__(self, x, topk_idx, topk_weights, out=None, err=None, stream=None):
+        """Enqueue the chunked forward on `stream` (default: current); returns out [T,H] bf16."""
+        if out is None:
+            out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=x.device)
+        err = err if err is not None else error_word(x.device)
+        ep_dispatch_chunked_forward_nosync(x, topk_idx, topk_weights, self.T, self.K, self.H, self.P, self.El,
+                                           self.chunks, int(self.fp8), self._cb, None, out, self.buffers, err,
+                                           stream, self.aux)
+        return out
+
+
+def dispatch_chunked_forward_nosync(x, topk_idx, topk_weights, *, num_local_experts: int, num_ranks: int,
+                                    chunks: int, fp8: bool = False, local_kernel=None, n_sets: int = 2, err=None,
+                                    stream=None):
+    """One call of the no-sync chunked forward (see ChunkedForward)."""
+    T, H = x.shape
+    f = ChunkedForward(T, topk_idx.shape[1], H, num_ranks=num_ranks, num_local_experts=num_local_experts,
+                       chunks=chunks, fp8=fp8, n_sets=n_sets, local_kernel=local_kernel, device=x.device)
+    out = f(x, topk_idx, topk_weights, err=err, stream=stream)
+    torch.cuda.synchronize(x.device)   # the buffers of f die with this call
     return out

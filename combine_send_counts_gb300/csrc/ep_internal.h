@@ -42,4 +42,10 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
                          int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
                          void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream);
 
+// The synthetic fp8 expert over N rows (ep_move.cu); with n_rows non-NULL,
+// rows at or past the device value *n_rows are skipped.
+int launch_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,
+                            const float *send_w, int64_t N, const int32_t *n_rows, int K, int H, void *out,
+                            cudaStream_t stream);
+
 }  // namespace ep

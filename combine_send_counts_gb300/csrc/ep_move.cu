@@ -192,58 +192,97 @@ __global__ void zero_pad_kernel(uint4 *__restrict__ b_x, const int32_t *__restri
 }
 
 // -------------------------------------------------- synthetic fp8 expert --
-// One block per row: d = e4m3(q) * scale, y_k = bf16(d * (1 + l_k/64)),
+// d = e4m3(q) * scale, y_k = bf16(d * (1 + l_k/64)),
 // out = bf16(fma over k ascending of w_k * y_k from +0.0f).
-__global__ void __launch_bounds__(256)
+// One warp per row, 8 rows per block: the lanes load the row's K expert ids
+// and weights at once and compact the ones in use (ascending k, by ballot)
+// into shared memory; each lane then issues kLocalU 16-byte code loads before
+// it converts any, so that enough bytes are in flight to keep HBM busy, and
+// applies the experts one at a time to all 16 values of a vector (16
+// independent fma chains; each value's chain still runs over k ascending).
+constexpr int kLocalRowsPerBlock = 8;
+constexpr int kLocalU = 4;
+
+__global__ void __launch_bounds__(kLocalRowsPerBlock * 32)
 local_expert_fp8_kernel(const uint4 *__restrict__ q, const float *__restrict__ scale,
-                        const int64_t *__restrict__ send_idx, const float *__restrict__ send_w,
-                        int64_t N, int K, int H, uint4 *__restrict__ out)
+                        const int64_t *__restrict__ send_idx, const float *__restrict__ send_w, int64_t N,
+                        const int32_t *__restrict__ n_rows, int K, int H, uint4 *__restrict__ out)
 {
-    __shared__ float s_fac[EP_MAX_TOPK];
-    __shared__ float s_w[EP_MAX_TOPK];
-    __shared__ int s_n;
-    const int64_t n = blockIdx.x;
-    if (threadIdx.x == 0) {
-        int m = 0;
-        for (int k = 0; k < K; ++k) {
-            const int64_t l = send_idx[n * K + k];
-            if (l >= 0) {
-                s_fac[m] = __fadd_rn(1.0f, __fmul_rn((float)l, 0.015625f));
-                s_w[m] = send_w[n * K + k];
-                ++m;
-            }
-        }
-        s_n = m;
+    __shared__ float s_fac[kLocalRowsPerBlock][EP_MAX_TOPK];
+    __shared__ float s_w[kLocalRowsPerBlock][EP_MAX_TOPK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * kLocalRowsPerBlock + warp;
+    int64_t lim = N;
+    if (n_rows != nullptr)   // rows past the device count are not in use
+        lim = min(lim, (int64_t)*n_rows);
+    if (n >= lim)
+        return;   // the whole warp
+    int64_t l = -1;
+    float wk = 0.0f;
+    if (lane < K) {
+        l = send_idx[n * K + lane];
+        wk = send_w[n * K + lane];
     }
-    __syncthreads();
-    const int m = s_n;
-    const int chunks = H / 16;   // 16 codes per 16-byte vector
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-        const uint4 v = q[n * chunks + c];
-        const float sc = scale[n * (H / 128) + c / 8];
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-        uint32_t packed[8];
+    const bool use = lane < K && l >= 0;
+    const unsigned used = __ballot_sync(kFull, use);
+    if (use) {
+        const int j = __popc(used & lanemask_lt());
+        s_fac[warp][j] = __fadd_rn(1.0f, __fmul_rn((float)l, 0.015625f));
+        s_w[warp][j] = wk;
+    }
+    __syncwarp();
+    const int m = __popc(used);
+    const float *fac = s_fac[warp], *wt = s_w[warp];
+    const int V = H / 16;   // 16 codes per 16-byte vector
+    const uint4 *qr = q + n * V;
+    const float *sr = scale + n * (H / 128);
+    uint4 *orow = out + n * V * 2;
+    for (int base = 0; base < V; base += 32 * kLocalU) {
+        uint4 v[kLocalU];
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(words[wi] >> (16 * hh));
-                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-                const float2 d2 = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-                const float d0 = __fmul_rn(d2.x, sc), d1 = __fmul_rn(d2.y, sc);
-                float a0 = 0.0f, a1 = 0.0f;
-                for (int k = 0; k < m; ++k) {
-                    const float y0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(d0, s_fac[k])));
-                    const float y1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(d1, s_fac[k])));
-                    a0 = __fmaf_rn(s_w[k], y0, a0);
-                    a1 = __fmaf_rn(s_w[k], y1, a1);
-                }
-                packed[wi * 2 + hh] = pack_bf16x2(a0, a1);
-            }
+        for (int u = 0; u < kLocalU; ++u) {
+            const int c = base + u * 32 + lane;
+            if (c < V)
+                v[u] = ld_stream(qr + c);
+            else
+                v[u] = make_uint4(0, 0, 0, 0);
         }
-        uint4 *o = out + (n * chunks + c) * 2;
-        o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+#pragma unroll
+        for (int u = 0; u < kLocalU; ++u) {
+            const int c = base + u * 32 + lane;
+            if (c >= V)
+                break;
+            const float sc = __ldg(sr + c / 8);
+            const uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            float d[16], a[16];
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(words[wi] >> (16 * hh));
+                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+                    const float2 d2 = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                    d[wi * 4 + hh * 2] = __fmul_rn(d2.x, sc);
+                    d[wi * 4 + hh * 2 + 1] = __fmul_rn(d2.y, sc);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                a[e] = 0.0f;
+            // experts outermost: 16 independent accumulation chains per step
+            for (int k = 0; k < m; ++k) {
+                const float f = fac[k], w = wt[k];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    a[e] = __fmaf_rn(w, __bfloat162float(__float2bfloat16_rn(__fmul_rn(d[e], f))), a[e]);
+            }
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                packed[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+            st_stream(orow + 2 * c, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+            st_stream(orow + 2 * c + 1, make_uint4(packed[4], packed[5], packed[6], packed[7]));
+        }
     }
 }
 
@@ -391,12 +430,11 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
     return EP_OK;
 }
 
-extern "C" int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,
-                                   const float *send_w, int64_t N, int K, int H, void *out, int32_t *err,
-                                   ep_stream_t stream_)
+namespace ep {
+int launch_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,
+                            const float *send_w, int64_t N, const int32_t *n_rows, int K, int H, void *out,
+                            cudaStream_t stream)
 {
-    (void)err;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (N < 0 || N >= ((int64_t)1 << 31) || K < 1 || K > EP_MAX_TOPK || H < 128 || H % 128 != 0)
         return EP_ERR_INVALID_ARG;
     if (N == 0)
@@ -404,8 +442,18 @@ extern "C" int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scal
     if (recv_q == nullptr || recv_scale == nullptr || send_idx == nullptr || send_w == nullptr ||
         out == nullptr || !aligned(recv_q, 16) || !aligned(out, 16))
         return EP_ERR_INVALID_ARG;
-    local_expert_fp8_kernel<<<(unsigned)N, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(recv_q),
-                                                             recv_scale, send_idx, send_w, N, K, H,
-                                                             static_cast<uint4 *>(out));
+    local_expert_fp8_kernel<<<(unsigned)ceil_div(N, kLocalRowsPerBlock), kLocalRowsPerBlock * 32, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(recv_q), recv_scale, send_idx, send_w, N, n_rows, K, H,
+        static_cast<uint4 *>(out));
     return launch_status();
+}
+}  // namespace ep
+
+extern "C" int ep_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,
+                                   const float *send_w, int64_t N, int K, int H, void *out, int32_t *err,
+                                   ep_stream_t stream_)
+{
+    (void)err;
+    return launch_local_expert_fp8(recv_q, recv_scale, send_idx, send_w, N, nullptr, K, H, out,
+                                   reinterpret_cast<cudaStream_t>(stream_));
 }

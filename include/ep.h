@@ -287,6 +287,76 @@ int ep_local_expert_fp8_callback(void *user, int chunk, int64_t n_rows, int K, i
                                  const int64_t *send_idx, const float *send_w, void *local_out,
                                  int32_t *err, ep_stream_t stream);
 
+/* [AX] dispatch_chunked_forward without a host round trip, pipelined over
+ * two streams: the pages overlap chunk i+1's all-to-alls with chunk i's expert
+ * compute, and [UB] Buffer.dispatch's "num_worst_tokens" mode sizes the
+ * receive buffers for the worst case so that nothing waits on the CPU.  Per
+ * chunk c (the token range of [AX] chunk_bounds):
+ *   on aux_stream: ep_route_nosync (num_worst_rows = b->max_rows), ep_dispatch
+ *     (bf16, or fp8 when fp8 = 1) into row set c % n_sets;
+ *   on stream: local_kernel, then ep_combine into the chunk's rows of
+ *     out [T,H] bf16.
+ * With two row sets, chunk c+1's routing and dispatch run while chunk c's
+ * local kernel and combine do; events order each set's reuse.  With one set
+ * (aux_stream may then be NULL) everything runs in order on `stream`.  The
+ * call never waits on the host, so it may be captured in a CUDA graph (stream
+ * must be the capturing stream; aux_stream joins the capture through events)
+ * and replayed on new inputs.  The results equal those of
+ * ep_dispatch_chunked_forward with the same local kernel.
+ *   local_kernel: as for ep_dispatch_chunked_forward, but it receives the row
+ *     capacity max_rows and a DEVICE pointer n_rows to the chunk's row count
+ *     (rank_offsets[c, P]); it must leave rows at or past *n_rows alone (they
+ *     hold stale data) and enqueue only on `stream`.
+ *     ep_local_expert_fp8_dev_callback is the synthetic fp8 expert in this form.
+ *   b->max_rows: rows of every row set; (longest chunk) * min(K, P) never
+ *     drops.  A chunk with more rows sets EP_ERR_CAPACITY on the device, and
+ *     its rows past max_rows are neither dispatched nor combined.
+ *   b->ws: ep_workspace_size(T, K, P, E_local, chunks) bytes; b->combine_ws:
+ *     EP_COMBINE_WS_BYTES bytes or NULL.  Both are used by one stream each.
+ * Returns the first non-OK status of the calls it makes; device errors go to
+ * err as for the calls above. */
+typedef int (*ep_local_kernel_dev_fn)(void *user, int chunk, int64_t max_rows, const int32_t *n_rows, int K,
+                                      int H, const void *recv_x, const float *recv_scale,
+                                      const int64_t *send_idx, const float *send_w, void *local_out,
+                                      int32_t *err, ep_stream_t stream);
+
+typedef struct ep_row_set {
+    int32_t *send_token_idx;   /* [max_rows] */
+    int32_t *send_rank;        /* [max_rows] */
+    int64_t *send_idx;         /* [max_rows,K] */
+    float *send_w;             /* [max_rows,K] */
+    void *recv_x;              /* [max_rows,H] bf16, or e4m3 when fp8 */
+    float *recv_scale;         /* [max_rows,H/128] when fp8, else NULL */
+    void *local_out;           /* [max_rows,H] bf16 */
+} ep_row_set;
+
+typedef struct ep_pipeline_buffers {
+    int32_t *dest;             /* [T,K] */
+    uint8_t *is_in_rank;       /* [T,P] */
+    int32_t *send_counts;      /* [chunks,P] */
+    int32_t *rank_offsets;     /* [chunks,P+1] */
+    int32_t *token_pos;        /* [T,P] */
+    int64_t max_rows;
+    int n_sets;                /* 1 or 2 */
+    ep_row_set sets[2];        /* chunk c uses sets[c % n_sets] */
+    void *ws;
+    size_t ws_bytes;
+    void *combine_ws;
+} ep_pipeline_buffers;
+
+int ep_dispatch_chunked_forward_nosync(const void *x, const int64_t *topk_idx, const float *topk_weights,
+                                       int64_t T, int K, int H, int P, int E_local, int chunks, int fp8,
+                                       ep_local_kernel_dev_fn local_kernel, void *user, void *out,
+                                       const ep_pipeline_buffers *b, int32_t *err, ep_stream_t stream,
+                                       ep_stream_t aux_stream);
+
+/* ep_local_expert_fp8 in the ep_local_kernel_dev_fn shape: max_rows blocks,
+ * rows at or past *n_rows skipped (user and chunk unused). */
+int ep_local_expert_fp8_dev_callback(void *user, int chunk, int64_t max_rows, const int32_t *n_rows, int K,
+                                     int H, const void *recv_x, const float *recv_scale,
+                                     const int64_t *send_idx, const float *send_w, void *local_out,
+                                     int32_t *err, ep_stream_t stream);
+
 /* Same as ep_compute_send_counts, but the caller passes no workspace: the
  * scratch lives in one fixed device array of EP_NOALLOC_SCRATCH_BYTES that the
  * library holds on every device that loads it, until the process exits.  The

@@ -87,3 +87,33 @@ def test_no_entry_point_host_code_calls_exit(lib):
         elif re.search(r"\s(call|bl|jmp|b)\s+[0-9a-f]+ <exit@plt>", line):
             offenders.add(fn)
     assert not offenders, offenders
+
+
+def test_ctypes_structs_match_the_header(tmp_path):
+    # Compile a probe against include/ep.h with the host C compiler and compare
+    # every struct's size and field offsets with the ctypes mirrors.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    mirrors = {"ep_chunk_buffers": ep.EPChunkBuffers, "ep_row_set": ep.EPRowSet,
+               "ep_pipeline_buffers": ep.EPPipelineBuffers}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "ep.h"', "int main(void) {"]
+    for cname, cls in mirrors.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0; }"]
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        cname, field, v = line.split()
+        got[(cname, field)] = int(v)
+    for cname, cls in mirrors.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)

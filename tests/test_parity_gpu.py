@@ -500,6 +500,127 @@ def test_chunked_driver_fp8_full_size_sampled():
         assert_combine_parity(f"token {t}", outb[t:t + 1], want)
 
 
+# ------------------------------------------- chunked forward without host sync --
+@pytest.mark.parametrize("n_sets", [1, 2])
+def test_chunked_nosync_fp8_matches_oracle_and_sync_driver(n_sets):
+    w = wl.WORKLOADS["chunk_fp8"].scaled(T=2048 + 37)
+    x, idx, wts = wl.make(w)
+    xd, idd, wd = x.cuda(), idx.cuda(), wts.cuda()
+    err = ep.error_word()
+    out = ep.dispatch_chunked_forward_nosync(xd, idd, wd, num_local_experts=w.E_local, num_ranks=w.P,
+                                             chunks=w.chunks, fp8=True, n_sets=n_sets, err=err)
+    ref = ep.dispatch_chunked_forward(xd, idd, wd, num_local_experts=w.E_local, num_ranks=w.P, chunks=w.chunks,
+                                      fp8=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_equal("nosync == sync driver", bits16(out), bits16(ref))
+    assert_combine_parity("chunked fp8 nosync", bits16(out),
+                          _oracle_chunked(x, idx, wts, w.P, w.E_local, w.chunks, True))
+
+
+@pytest.mark.parametrize("n_sets", [1, 2])
+def test_chunked_nosync_bf16_python_local_kernel(n_sets):
+    w = dataclasses.replace(wl.WORKLOADS["mid"].scaled(T=1500), chunks=5)
+    x, idx, wts = wl.make(w)
+    seen = []
+
+    def identity(chunk, recv_x, recv_scale, send_idx, send_w, local_out, n_rows):
+        seen.append(chunk)
+        assert recv_scale is None and n_rows.numel() == 1 and n_rows.is_cuda
+        local_out.copy_(recv_x)                      # rows past n_rows are never combined
+
+    err = ep.error_word()
+    out = ep.dispatch_chunked_forward_nosync(x.cuda(), idx.cuda(), wts.cuda(), num_local_experts=w.E_local,
+                                             num_ranks=w.P, chunks=w.chunks, local_kernel=identity, n_sets=n_sets,
+                                             err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert seen == list(range(w.chunks))
+    assert_combine_parity("chunked bf16 nosync", bits16(out),
+                          _oracle_chunked(x, idx, wts, w.P, w.E_local, w.chunks, False))
+
+
+def test_chunked_nosync_graph_replays_new_inputs():
+    w = wl.WORKLOADS["chunk_fp8"].scaled(T=1024 + 5)
+    f = ep.ChunkedForward(w.T, w.K, w.H, num_ranks=w.P, num_local_experts=w.E_local, chunks=w.chunks, fp8=True,
+                          n_sets=2)
+    xs = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((w.T, w.K), dtype=torch.int64, device="cuda")
+    ws_ = torch.empty((w.T, w.K), dtype=torch.float32, device="cuda")
+    out = torch.empty_like(xs)
+    err = ep.error_word()
+    x0, i0, w0 = wl.make(w)
+    xs.copy_(x0)
+    ids.copy_(i0)
+    ws_.copy_(w0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        f(xs, ids, ws_, out=out, err=err)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        f(xs, ids, ws_, out=out, err=err)
+    torch.cuda.synchronize()
+    for seed in (11, 12, 13):
+        wi = dataclasses.replace(w, seed=seed)
+        x, idx, wts = wl.make(wi)
+        xs.copy_(x)
+        ids.copy_(idx)
+        ws_.copy_(wts)
+        out.fill_(0)
+        err.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_combine_parity(f"replay seed {seed}", bits16(out),
+                              _oracle_chunked(x, idx, wts, w.P, w.E_local, w.chunks, True))
+
+
+def test_chunked_nosync_capacity_is_flagged():
+    w = wl.WORKLOADS["chunk_fp8"].scaled(T=1024)
+    x, idx, wts = wl.make(w)
+    f = ep.ChunkedForward(w.T, w.K, w.H, num_ranks=w.P, num_local_experts=w.E_local, chunks=w.chunks, fp8=True,
+                          n_sets=2, max_rows=64)       # far fewer rows than any chunk uses
+    err = ep.error_word()
+    f(x.cuda(), idx.cuda(), wts.cuda(), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ep.EP_ERR_CAPACITY
+    for c in range(w.chunks):                         # the true counts are still reported
+        assert int(f.t["rank_offsets"][c, w.P].item()) > 64
+    assert int(f.t["token_pos"].max().item()) < 64    # nothing placed past the capacity
+
+
+def test_chunked_nosync_empty():
+    f = ep.ChunkedForward(0, 8, 256, num_ranks=4, num_local_experts=2, chunks=3, fp8=True, n_sets=2)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((0, 8), dtype=torch.int64, device="cuda")
+    wts = torch.empty((0, 8), dtype=torch.float32, device="cuda")
+    err = ep.error_word()
+    out = f(x, idx, wts, err=err)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256) and int(err.item()) == 0
+    assert int(f.t["rank_offsets"].abs().sum().item()) == 0
+
+
+def test_chunked_nosync_full_size_sampled():
+    w = wl.WORKLOADS["chunk_fp8"]
+    x, idx, wts = wl.make(w)
+    err = ep.error_word()
+    out = ep.dispatch_chunked_forward_nosync(x.cuda(), idx.cuda(), wts.cuda(), num_local_experts=w.E_local,
+                                             num_ranks=w.P, chunks=w.chunks, fp8=True, n_sets=2, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    outb = bits16(out)
+    g = np.random.Generator(np.random.PCG64(322))
+    for t in np.sort(g.choice(w.T, size=64, replace=False)).tolist():
+        r = oracle.send_path(x[t:t + 1], idx[t:t + 1], wts[t:t + 1], None, w.P, w.E_local)
+        lay = r["layout"]
+        q, sc = oracle.dispatch_fp8(x[t:t + 1], lay["send_token_idx"])
+        want = oracle.combine(oracle.local_expert_fp8(q, sc, lay["send_idx"], lay["send_w"]), lay["token_pos"])
+        assert_combine_parity(f"token {t}", outb[t:t + 1], want)
+
+
 # ----------------------------------------- items with more sources than buffers --
 # With H = 7168 the combine's shared-memory ring holds 8 rows; these cases give
 # every token 16 or 32 source rows, so each item reuses ring buffers within
