@@ -67,6 +67,8 @@ def _load():
         "orc_combine": (None, [P, i64, i32, i32, P, i32, P]),
         "orc_batched_prepare": (i32, [P, P, i64, i32, i32, i32, i32, i32, i32, P, P, P, i32]),
         "orc_batched_combine": (None, [P, P, P, P, i64, i32, i32, i32, i32, i32, P]),
+        "orc_quantize_fp8_rows_pow2": (None, [P, i64, i32, P, P, P]),
+        "orc_batched_prepare_fp8": (i32, [P, P, i64, i32, i32, i32, i32, i32, i32, P, P, i32, i32, P, P, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -181,6 +183,50 @@ def quantize_fp8_rows(x):
     s = np.empty((R, H // 128), np.float32)
     _load().orc_quantize_fp8_rows(_ptr(xb), R, H, _ptr(q), _ptr(s))
     return q, s
+
+
+def quantize_fp8_rows_pow2(x):
+    """Power-of-two group scales: -> (codes [R,H] u8, scales [R,H/128] f32, UE8M0 codes [R,H/128] u8)."""
+    xb = _bf16_bits(x)
+    R, H = xb.shape
+    q = np.empty((R, H), np.uint8)
+    s = np.empty((R, H // 128), np.float32)
+    c = np.empty((R, H // 128), np.uint8)
+    _load().orc_quantize_fp8_rows_pow2(_ptr(xb), R, H, _ptr(q), _ptr(s), _ptr(c))
+    return q, s, c
+
+
+SCALE_ROW_F32, SCALE_COL_F32, SCALE_COL_UE8M0 = 0, 1, 2
+
+
+def batched_scale_shape(E_local: int, M: int, H: int, fmt: int):
+    """Storage shape and dtype of the batched scales of each format (fmt 1 and
+    2 are column-major in their last two dims, stored as [E_local, G, M])."""
+    G = H // 128
+    if fmt == SCALE_ROW_F32:
+        return (E_local, M, G), np.float32
+    if fmt == SCALE_COL_F32:
+        return (E_local, G, M), np.float32
+    return (E_local, G // 4, M), np.int32
+
+
+def batched_prepare_fp8(x, topk_idx, E: int, E_local: int, rank: int, M: int, fmt: int = SCALE_ROW_F32,
+                        round_scale: bool = False, zero_pad: bool = False, b_q_init=None, b_scale_init=None):
+    """-> dict(b_q [E_local,M,H] u8, b_scale (storage layout of batched_scale_shape),
+    tokens_per_expert, slot, err)."""
+    xb = _bf16_bits(x)
+    idx = _c(topk_idx, np.int64)
+    T, H = xb.shape
+    K = idx.shape[1]
+    shape, dt = batched_scale_shape(E_local, M, H, fmt)
+    b_q = np.zeros((E_local, M, H), np.uint8) if b_q_init is None else np.array(b_q_init, np.uint8, copy=True)
+    b_s = np.zeros(shape, dt) if b_scale_init is None else np.array(b_scale_init, dt, copy=True)
+    tpe = np.empty(E_local, np.int32)
+    slot = np.empty((T, K), np.int32)
+    err = _load().orc_batched_prepare_fp8(_ptr(xb), _ptr(idx), T, K, H, E, E_local, rank, M, _ptr(b_q),
+                                          _ptr(b_s), int(fmt), int(round_scale), _ptr(tpe), _ptr(slot),
+                                          int(zero_pad))
+    return dict(b_q=b_q, b_scale=b_s, tokens_per_expert=tpe, slot=slot, err=int(err))
 
 
 def dispatch_fp8(x, send_token_idx):

@@ -14,7 +14,9 @@
  *   [UB]  NeMo AutoModel docs, nemo_automodel.components.moe.uccl_ep.buffer:
  *         Buffer.get_dispatch_layout, Buffer.dispatch (fp8 payload: e4m3
  *         [T,H] + fp32 scales [T,H/128]), Buffer.combine (addition without
- *         weights), Buffer.low_latency_combine (reduce with weights).
+ *         weights), Buffer.low_latency_dispatch (round_scale, use_ue8m0,
+ *         column-major scales), Buffer.low_latency_combine (reduce with
+ *         weights).
  *   [VB]  vLLM docs, vllm.model_executor.layers.fused_moe.prepare_finalize:
  *         BatchedPrepareAndFinalize.prepare (hit mask, tokens_per_expert,
  *         slots that preserve token order) and .finalize.
@@ -38,7 +40,11 @@
  *     round-to-nearest-even;
  *   - chunk_bounds: chunk size floor(T / C); the last chunk takes the rest;
  *   - expert-batched capacity: a token past max_num_tokens is dropped (slot
- *     -1, row not written), tokens_per_expert is clipped, error bit 8.
+ *     -1, row not written), tokens_per_expert is clipped, error bit 8;
+ *   - power-of-two scales (round_scale): the smallest power of two >= a/448,
+ *     so x / scale never exceeds 448; the UE8M0 code is its biased exponent;
+ *     four codes pack into an int32 with group 4j+i at byte i (least
+ *     significant first).
  *
  * Build: plain C11, -O2 -fno-fast-math -ffp-contract=off (no contraction of
  * a*b+c, so every rounding is the one written here).
@@ -446,4 +452,134 @@ void orc_batched_combine(const uint16_t *y, const int64_t *topk_idx, const float
             out[t * H + h] = orc_f32_to_bf16(acc[h]);
     }
     free(acc);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Power-of-two group scales ([UB] Buffer.low_latency_dispatch, round_scale:  */
+/* "round the scaling factors into power of 2"; use_ue8m0: the scale as an    */
+/* UE8M0 code).  Per row and 128-element group g:                            */
+/*   a      = max(max_i |x_i|, 1e-4f)                                        */
+/*   s0     = a / 448.0f                    (fp32, nearest-even)             */
+/*   scale  = the smallest power of two >= s0  (reading: rounding up keeps   */
+/*            every |x_i| / scale <= 448, so nothing saturates)              */
+/*   q_i    = e4m3_rn_satfinite(x_i * (1 / scale))   (1/scale is exact)      */
+/*   code   = e + 127 where scale = 2^e (UE8M0: 8 exponent bits, bias 127,   */
+/*            no sign, no mantissa)                                          */
+/* ------------------------------------------------------------------------ */
+void orc_quantize_fp8_rows_pow2(const uint16_t *x, int64_t rows, int H, uint8_t *q, float *scale,
+                                uint8_t *code)
+{
+    int G = H / 128;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int g = 0; g < G; ++g) {
+            const uint16_t *xs = x + r * H + (int64_t)g * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                float v = fabsf(orc_bf16_to_f32(xs[i]));
+                if (v > amax)
+                    amax = v;
+            }
+            float a = amax > 1e-4f ? amax : 1e-4f;
+            float s0 = a / 448.0f;
+            int e;
+            float m = frexpf(s0, &e);        /* s0 = m * 2^e, 0.5 <= m < 1 */
+            if (m == 0.5f)
+                e -= 1;                      /* s0 is itself a power of two */
+            float sc = ldexpf(1.0f, e);
+            float inv = ldexpf(1.0f, -e);
+            for (int i = 0; i < 128; ++i)
+                q[r * H + (int64_t)g * 128 + i] = orc_f32_to_e4m3(orc_bf16_to_f32(xs[i]) * inv);
+            scale[r * G + g] = sc;
+            code[r * G + g] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* [VB] BatchedPrepareAndFinalize.prepare, quantised branch, with the scale   */
+/* layouts of [UB] Buffer.low_latency_dispatch.  Slots, tokens_per_expert,   */
+/* capacity and error bits as orc_batched_prepare; each token is quantised   */
+/* once (1x128 groups; plain or power-of-two scales) and every slot it takes */
+/* carries the same codes.  With G = H/128 groups per row:                   */
+/*   fmt 0: scales [E_local, M, G] fp32, row-major: (e,s,g) at (e*M+s)*G+g;  */
+/*   fmt 1: scales [E_local, M, G] fp32, last two dims column-major:         */
+/*          (e,s,g) at (e*G+g)*M+s;                                          */
+/*   fmt 2: scales [E_local, M, G/4] int32, last two dims column-major:      */
+/*          (e,s,j) at (e*(G/4)+j)*M+s; byte (g mod 4) of int (e,s,g/4),     */
+/*          little-endian, is group g's UE8M0 code (needs round_scale).      */
+/* zero_pad: codes and scale entries of slots >= tokens_per_expert are set   */
+/* to zero (the page's zero-initialised outputs); otherwise left as given.   */
+/* Returns error bits; 16 (unsupported) for fmt 2 without round_scale or     */
+/* H % 512 != 0.                                                             */
+/* ------------------------------------------------------------------------ */
+int orc_batched_prepare_fp8(const uint16_t *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
+                            int E_local, int rank, int M, uint8_t *b_q, void *b_scale, int fmt,
+                            int round_scale, int32_t *tokens_per_expert, int32_t *slot, int zero_pad)
+{
+    int G = H / 128;
+    if (fmt == 2 && (!round_scale || H % 512 != 0))
+        return 16;
+    uint8_t *q = (uint8_t *)malloc((size_t)(T > 0 ? T : 1) * H);
+    float *sc = (float *)malloc((size_t)(T > 0 ? T : 1) * G * sizeof(float));
+    uint8_t *code = (uint8_t *)malloc((size_t)(T > 0 ? T : 1) * G);
+    if (round_scale)
+        orc_quantize_fp8_rows_pow2(x, T, H, q, sc, code);
+    else
+        orc_quantize_fp8_rows(x, T, H, q, sc);
+    float *sf = (float *)b_scale;
+    uint8_t *sb = (uint8_t *)b_scale;
+    int err = 0;
+    for (int64_t i = 0; i < T * K; ++i) {
+        slot[i] = -1;
+        int64_t id = topk_idx[i];
+        if (id < -1 || id >= E)
+            err |= ORC_ERR_INVALID_EXPERT;
+    }
+    for (int el = 0; el < E_local; ++el) {
+        int64_t e = (int64_t)rank * E_local + el;
+        int64_t s = 0;
+        for (int64_t t = 0; t < T; ++t) {
+            int hit = 0;
+            for (int k = 0; k < K; ++k)
+                if (topk_idx[t * K + k] == e)
+                    hit = 1;
+            if (!hit)
+                continue;
+            if (s < M) {
+                memcpy(b_q + ((int64_t)el * M + s) * H, q + t * H, (size_t)H);
+                for (int g = 0; g < G; ++g) {
+                    if (fmt == 0)
+                        sf[((int64_t)el * M + s) * G + g] = sc[t * G + g];
+                    else if (fmt == 1)
+                        sf[((int64_t)el * G + g) * M + s] = sc[t * G + g];
+                    else
+                        sb[(((int64_t)el * (G / 4) + g / 4) * M + s) * 4 + g % 4] = code[t * G + g];
+                }
+                for (int k = 0; k < K; ++k)
+                    if (topk_idx[t * K + k] == e)
+                        slot[t * K + k] = (int32_t)s;
+            } else {
+                err |= ORC_ERR_CAPACITY;
+            }
+            ++s;
+        }
+        int32_t c = (int32_t)(s < M ? s : M);
+        tokens_per_expert[el] = c;
+        if (zero_pad) {
+            memset(b_q + ((int64_t)el * M + c) * H, 0, (size_t)(M - c) * H);
+            for (int64_t r = c; r < M; ++r)
+                for (int g = 0; g < G; ++g) {
+                    if (fmt == 0)
+                        sf[((int64_t)el * M + r) * G + g] = 0.0f;
+                    else if (fmt == 1)
+                        sf[((int64_t)el * G + g) * M + r] = 0.0f;
+                    else
+                        sb[(((int64_t)el * (G / 4) + g / 4) * M + r) * 4 + g % 4] = 0;
+                }
+        }
+    }
+    free(q);
+    free(sc);
+    free(code);
+    return err;
 }
