@@ -499,6 +499,18 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
         y, idx, wts, r["slot"], w.T, w.K, w.H, w.E_local, w.rank, w.max_num_tokens, o, cws, err), iters)
     out["batched_combine"] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab,
                               "gbs": round(ab / us / 1e3, 1), "frac": round(ab / us / 1e3 / peak, 4)}
+    # fp8 expert-batched prepare: codes + column-major scales (fp32, or
+    # power-of-two UE8M0 packed four per int)
+    ab8 = w.T * w.H * 2 + hits * (w.H + w.H // 32)
+    for name, fmt, rs in (("batched_prepare_fp8_col_f32", ep.EP_SCALE_COL_F32, 0),
+                          ("batched_prepare_fp8_ue8m0", ep.EP_SCALE_COL_UE8M0, 1)):
+        r8 = ep.batched_prepare_fp8(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, fmt, bool(rs), err=err)
+        us = _event_time_us(torch, flush, lambda: ep.ep_batched_prepare_fp8(
+            x, idx, w.T, w.K, w.H, w.E, w.E_local, w.rank, w.max_num_tokens, r8["b_q"], r8["b_scale"], fmt, rs,
+            r8["tokens_per_expert"], r8["slot"], 0, ws, err), iters)
+        out[name] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab8,
+                     "gbs": round(ab8 / us / 1e3, 1), "frac": round(ab8 / us / 1e3 / peak, 4)}
+        del r8
     del x, y, o, r
 
     w = wl.WORKLOADS["chunk_fp8"]

@@ -74,7 +74,11 @@ _SIGNATURES = {
                                               _VP, _VP]),
     "ep_local_expert_fp8_dev_callback": (_I32, [_VP, _I32, _I64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                                                 _VP]),
+    "ep_batched_prepare_fp8": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _I32, _I32,
+                                      _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
 }
+
+EP_SCALE_ROW_F32, EP_SCALE_COL_F32, EP_SCALE_COL_UE8M0 = 0, 1, 2
 
 
 class EPChunkBuffers(ctypes.Structure):
@@ -225,6 +229,15 @@ def ep_batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b
                                    int(zero_pad), _p(ws), ws.numel() * ws.element_size(), _p(err),
                                    _stream(stream))
     _check(rc, "ep_batched_prepare")
+
+
+def ep_batched_prepare_fp8(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b_q, b_scale, scale_fmt,
+                           round_scale, tokens_per_expert, slot, zero_pad, ws, err, stream=None):
+    rc = load().ep_batched_prepare_fp8(_p(x), _p(topk_idx), int(T), int(K), int(H), int(E), int(E_local),
+                                       int(rank), int(max_num_tokens), _p(b_q), _p(b_scale), int(scale_fmt),
+                                       int(round_scale), _p(tokens_per_expert), _p(slot), int(zero_pad), _p(ws),
+                                       ws.numel() * ws.element_size(), _p(err), _stream(stream))
+    _check(rc, "ep_batched_prepare_fp8")
 
 
 def ep_batched_combine(y, topk_idx, topk_weights, slot, T, K, H, E_local, rank, max_num_tokens, out, ws, err,
@@ -455,6 +468,38 @@ def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank:
     ep_batched_prepare(x, topk_idx, T, K, H, num_experts, El, rank, max_num_tokens, b_x, tpe, slot,
                        int(zero_pad), ws, err, stream)
     return dict(b_x=b_x, tokens_per_expert=tpe, slot=slot, err=err)
+
+
+def batched_scale_storage(E_local: int, M: int, H: int, scale_fmt: int):
+    """(shape, dtype) of the scale tensor of each EP_SCALE_* layout, in storage
+    order: the column-major layouts are stored as [E_local, groups, M]."""
+    G = H // 128
+    if scale_fmt == EP_SCALE_ROW_F32:
+        return (E_local, M, G), torch.float32
+    if scale_fmt == EP_SCALE_COL_F32:
+        return (E_local, G, M), torch.float32
+    return (E_local, G // 4, M), torch.int32
+
+
+def batched_prepare_fp8(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int,
+                        scale_fmt: int = EP_SCALE_ROW_F32, round_scale: bool = False, zero_pad: bool = False,
+                        err=None, stream=None):
+    """-> dict(b_q [E_local,M,H] uint8 (e4m3 codes), b_scale (batched_scale_storage),
+    tokens_per_expert [E_local], slot [T,K])."""
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    El = num_local_experts
+    dev = x.device
+    b_q = torch.empty((El, max_num_tokens, H), dtype=torch.uint8, device=dev)
+    shape, dt = batched_scale_storage(El, max_num_tokens, H, scale_fmt)
+    b_s = torch.empty(shape, dtype=dt, device=dev)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws = workspace(T, K, num_experts // El, El, 1, dev)
+    err = err if err is not None else error_word(dev)
+    ep_batched_prepare_fp8(x, topk_idx, T, K, H, num_experts, El, rank, max_num_tokens, b_q, b_s, scale_fmt,
+                           int(round_scale), tpe, slot, int(zero_pad), ws, err, stream)
+    return dict(b_q=b_q, b_scale=b_s, tokens_per_expert=tpe, slot=slot, err=err)
 
 
 def batched_combine(y, topk_idx, topk_weights, slot, rank: int, err=None, stream=None, ws="auto"):

@@ -102,14 +102,52 @@ scatter_bf16_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows row
 }
 
 // ------------------------------------------------- fp8 (1x128) scatter --
+// Where and how the group scales go: the layout (EP_SCALE_*) and whether the
+// scales are powers of two.  Column-major layouts index destination row
+// r = e * M + s as (e, s).
+struct ScaleSpec {
+    void *out;
+    int fmt;
+    int round;
+    int M;
+};
+
+// Index of group 0's scale of destination row r (4-byte entries; bytes for
+// UE8M0), computed once per row; put_scale adds the group's offset.
+template <int SF>
+__device__ __forceinline__ int64_t scale_row_base(const ScaleSpec &sp, int32_t r, int groups)
+{
+    if (SF == EP_SCALE_ROW_F32)
+        return (int64_t)r * groups;
+    const int e = r / sp.M, s = r - e * sp.M;
+    if (SF == EP_SCALE_COL_F32)
+        return (int64_t)e * groups * sp.M + s;
+    return ((int64_t)e * (groups >> 2) * sp.M + s) * 4;
+}
+
+template <int SF>
+__device__ __forceinline__ void put_scale(const ScaleSpec &sp, int64_t base, int gi, float sc, uint32_t code)
+{
+    if (SF == EP_SCALE_ROW_F32)
+        static_cast<float *>(sp.out)[base + gi] = sc;
+    else if (SF == EP_SCALE_COL_F32)
+        static_cast<float *>(sp.out)[base + (int64_t)gi * sp.M] = sc;
+    else
+        static_cast<uint8_t *>(sp.out)[base + (int64_t)(gi >> 2) * sp.M * 4 + (gi & 3)] = (uint8_t)code;
+}
+
 // Quantises each source row once, in 128-element groups (16 vectors, held by
 // 16 consecutive lanes because G is a multiple of 32), and writes the e4m3
-// codes and the fp32 group scales to each destination row:
-//   a = max(max|x|, 1e-4), q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448.
-template <int U, class Rows>
+// codes and the group scales to each destination row.  With a = max(max|x|, 1e-4):
+//   plain:        q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448;
+//   power of two: scale = 2^e, the smallest power of two >= a / 448 (from the
+//                 bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
+//                 UE8M0 code e + 127.
+// SF: the scale layout (EP_SCALE_*); RS: power-of-two scales.
+template <int U, class Rows, int SF, bool RS>
 __global__ void __launch_bounds__(kMoveThreads)
 scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows, int64_t n_rows,
-                   int err_bits, uint2 *__restrict__ out_q, float *__restrict__ out_scale, int32_t *err)
+                   int err_bits, uint2 *__restrict__ out_q, ScaleSpec sp, int32_t *err)
 {
     __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
     const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
@@ -126,6 +164,7 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
     for (int base = 0; base < g.nvec; base += g.G * U) {
         uint2 q[U];
         float scale[U];
+        uint32_t code[U];
         uint4 vin[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {            // all loads first: U vectors in flight
@@ -147,7 +186,20 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
             for (int off = 8; off > 0; off >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
             const float a = fmaxf(amax, 1e-4f);
-            const float inv = __fdiv_rn(448.0f, a);
+            float inv;
+            if (RS) {
+                // a / 448 is a positive normal fp32: round its exponent up
+                // unless the mantissa is zero
+                const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
+                const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
+                scale[u] = __uint_as_float(eb << 23);
+                inv = __uint_as_float((254u - eb) << 23);
+                code[u] = eb;
+            } else {
+                inv = __fdiv_rn(448.0f, a);
+                scale[u] = __fdiv_rn(a, 448.0f);
+                code[u] = 0;
+            }
             uint32_t packed[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -155,21 +207,20 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
                 packed[e] = (uint32_t)__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
             }
             q[u] = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
-            scale[u] = __fdiv_rn(a, 448.0f);
         }
         for (int j = 0; j < D; ++j) {
             const int32_t r = list[j];
             if (r < 0)
                 continue;
             uint2 *dq = out_q + (int64_t)r * g.nvec;
-            float *ds = out_scale + (int64_t)r * groups;
+            const int64_t sb = scale_row_base<SF>(sp, r, groups);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int i = base + lt + u * g.G;
                 if (i < g.nvec) {
                     st_stream(dq + i, q[u]);
                     if ((lt & 15) == 0)
-                        ds[i >> 4] = scale[u];
+                        put_scale<SF>(sp, sb, i >> 4, scale[u], code[u]);
                 }
             }
         }
@@ -189,6 +240,22 @@ __global__ void zero_pad_kernel(uint4 *__restrict__ b_x, const int32_t *__restri
     for (int64_t i = first + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x)
         st_stream(base + i, z);
+}
+
+// Zero the scale entries of slots [tokens_per_expert[e], M) of every local
+// expert, in any scale layout (4-byte entries; UE8M0 ints hold 4 groups).
+__global__ void zero_pad_scales_kernel(ScaleSpec sp, const int32_t *__restrict__ tokens_per_expert, int groups)
+{
+    const int e = blockIdx.y;
+    const int first = tokens_per_expert[e];
+    const int per_row = sp.fmt == EP_SCALE_COL_UE8M0 ? groups / 4 : groups;
+    const int64_t total = (int64_t)sp.M * per_row;
+    uint32_t *base = static_cast<uint32_t *>(sp.out) + (int64_t)e * total;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t s = sp.fmt == EP_SCALE_ROW_F32 ? i / per_row : i % sp.M;
+        if (s >= first)
+            base[i] = 0u;
+    }
 }
 
 // -------------------------------------------------- synthetic fp8 expert --
@@ -319,10 +386,10 @@ static int launch_scatter_bf16(const void *x, int64_t T, int H, const Rows &rows
     return launch_status();
 }
 
-template <class Rows>
-static int launch_scatter_fp8(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
-                              int err_bits, void *out_q, float *out_scale, int32_t *err,
-                              cudaStream_t stream)
+template <class Rows, int SF, bool RS>
+static int launch_scatter_fp8_as(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
+                                 int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err,
+                                 cudaStream_t stream)
 {
     int U;
     const Geometry g = geometry_for(H / 8, U);
@@ -331,13 +398,40 @@ static int launch_scatter_fp8(const void *x, int64_t T, int H, const Rows &rows,
         return EP_OK;
     auto *xs = static_cast<const uint4 *>(x);
     auto *q = static_cast<uint2 *>(out_q);
+    const int nt = g.G * g.tpb;
     switch (U) {
-    case 8: scatter_fp8_kernel<8><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
-    case 4: scatter_fp8_kernel<4><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
-    case 2: scatter_fp8_kernel<2><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
-    default: scatter_fp8_kernel<1><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, out_scale, err); break;
+    case 8: scatter_fp8_kernel<8, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    case 4: scatter_fp8_kernel<4, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    case 2: scatter_fp8_kernel<2, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    default: scatter_fp8_kernel<1, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
     }
     return launch_status();
+}
+
+// The send layout only takes row-major plain scales.
+static int launch_scatter_fp8(const void *x, int64_t T, int H, const SendRows &rows, int64_t n_rows,
+                              int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream)
+{
+    return launch_scatter_fp8_as<SendRows, EP_SCALE_ROW_F32, false>(x, T, H, rows, n_rows, err_bits, out_q, sp,
+                                                                     err, stream);
+}
+
+static int launch_scatter_fp8(const void *x, int64_t T, int H, const BatchedRows &rows, int64_t n_rows,
+                              int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream)
+{
+    if (sp.fmt == EP_SCALE_COL_UE8M0)
+        return launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_UE8M0, true>(x, T, H, rows, n_rows, err_bits,
+                                                                            out_q, sp, err, stream);
+    if (sp.fmt == EP_SCALE_COL_F32)
+        return sp.round ? launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_F32, true>(x, T, H, rows, n_rows, err_bits,
+                                                                                     out_q, sp, err, stream)
+                        : launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_F32, false>(x, T, H, rows, n_rows,
+                                                                                      err_bits, out_q, sp, err,
+                                                                                      stream);
+    return sp.round ? launch_scatter_fp8_as<BatchedRows, EP_SCALE_ROW_F32, true>(x, T, H, rows, n_rows, err_bits,
+                                                                                 out_q, sp, err, stream)
+                    : launch_scatter_fp8_as<BatchedRows, EP_SCALE_ROW_F32, false>(x, T, H, rows, n_rows, err_bits,
+                                                                                  out_q, sp, err, stream);
 }
 
 static bool row_shape_ok(int64_t T, int H)
@@ -386,16 +480,17 @@ extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token
         return EP_OK;
     const SendRows rows{token_pos, P};
     if (fp8)
-        return launch_scatter_fp8(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, recv_scale, err, stream);
+        return launch_scatter_fp8(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x,
+                                  ScaleSpec{recv_scale, EP_SCALE_ROW_F32, 0, 0}, err, stream);
     return launch_scatter_bf16(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, err, stream);
 }
 
-extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
-                                  int E_local, int rank, int max_num_tokens, void *b_x,
-                                  int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws,
-                                  size_t ws_bytes, int32_t *err, ep_stream_t stream_)
+// bf16 rows (sp == nullptr) or fp8 codes with scales as *sp.
+static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E, int E_local,
+                           int rank, int max_num_tokens, void *b_x, const ScaleSpec *sp,
+                           int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws, size_t ws_bytes,
+                           int32_t *err, cudaStream_t stream)
 {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || E < E_local || E % E_local != 0)
         return EP_ERR_INVALID_ARG;
     if (rank < 0 || (int64_t)(rank + 1) * E_local > E || max_num_tokens < 0)
@@ -406,7 +501,8 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
         return EP_ERR_INVALID_ARG;
     if (T > 0 && (x == nullptr || topk_idx == nullptr || slot == nullptr || !aligned(x, 16)))
         return EP_ERR_INVALID_ARG;
-    if ((int64_t)E_local * max_num_tokens > 0 && (b_x == nullptr || !aligned(b_x, 16)))
+    if ((int64_t)E_local * max_num_tokens > 0 &&
+        (b_x == nullptr || !aligned(b_x, 16) || (sp != nullptr && (sp->out == nullptr || !aligned(sp->out, 4)))))
         return EP_ERR_INVALID_ARG;
     if (ws_bytes < kWsAlign + (size_t)ceil_div(T, kRouteThreads) * E_local * sizeof(int32_t))
         return EP_ERR_INVALID_ARG;
@@ -417,17 +513,53 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
         return rc;
     if (T > 0) {
         const BatchedRows rows{topk_idx, slot, nullptr, K, (int64_t)rank * E_local, E_local, max_num_tokens, true};
-        rc = launch_scatter_bf16(x, T, H, rows, (int64_t)E_local * max_num_tokens, EP_ERR_CAPACITY, b_x, err, stream);
+        const int64_t n_rows = (int64_t)E_local * max_num_tokens;
+        rc = sp == nullptr ? launch_scatter_bf16(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, err, stream)
+                           : launch_scatter_fp8(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, *sp, err, stream);
         if (rc != EP_OK)
             return rc;
     }
     if (zero_pad && max_num_tokens > 0) {
-        dim3 grid((unsigned)std::min<int64_t>(ceil_div((int64_t)max_num_tokens * (H / 8), 256), 1024), E_local);
-        zero_pad_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), tokens_per_expert,
-                                                  max_num_tokens, H / 8);
-        return launch_status();
+        const int nvec = sp == nullptr ? H / 8 : H / 16;   // 16-byte vectors per row
+        dim3 grid((unsigned)std::min<int64_t>(ceil_div((int64_t)max_num_tokens * nvec, 256), 1024), E_local);
+        zero_pad_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), tokens_per_expert, max_num_tokens,
+                                                  nvec);
+        if ((rc = launch_status()) != EP_OK)
+            return rc;
+        if (sp != nullptr) {
+            dim3 sgrid((unsigned)std::min<int64_t>(ceil_div((int64_t)max_num_tokens * (H / 128), 256), 256),
+                       E_local);
+            zero_pad_scales_kernel<<<sgrid, 256, 0, stream>>>(*sp, tokens_per_expert, H / 128);
+            return launch_status();
+        }
     }
     return EP_OK;
+}
+
+extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
+                                  int E_local, int rank, int max_num_tokens, void *b_x,
+                                  int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws,
+                                  size_t ws_bytes, int32_t *err, ep_stream_t stream)
+{
+    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b_x, nullptr,
+                           tokens_per_expert, slot, zero_pad, ws, ws_bytes, err,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ep_batched_prepare_fp8(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
+                                      int E_local, int rank, int max_num_tokens, uint8_t *b_q, void *b_scale,
+                                      int scale_fmt, int round_scale, int32_t *tokens_per_expert, int32_t *slot,
+                                      int zero_pad, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream)
+{
+    if (scale_fmt != EP_SCALE_ROW_F32 && scale_fmt != EP_SCALE_COL_F32 && scale_fmt != EP_SCALE_COL_UE8M0)
+        return EP_ERR_INVALID_ARG;
+    if (round_scale != 0 && round_scale != 1)
+        return EP_ERR_INVALID_ARG;
+    if (H % 128 != 0 || (scale_fmt == EP_SCALE_COL_UE8M0 && (!round_scale || H % 512 != 0)))
+        return EP_ERR_UNSUPPORTED;
+    const ScaleSpec sp{b_scale, scale_fmt, round_scale, max_num_tokens};
+    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b_q, &sp, tokens_per_expert,
+                           slot, zero_pad, ws, ws_bytes, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 namespace ep {

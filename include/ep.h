@@ -208,6 +208,41 @@ int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K,
                        void *b_x, int32_t *tokens_per_expert, int32_t *slot, int zero_pad,
                        void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
 
+/* Scale layouts of ep_batched_prepare_fp8 ([UB] Buffer.low_latency_dispatch
+ * returns the scales of the expert-batched fp8 payload with the last two
+ * dimensions column-major; [VB] prepare's batched scale shape is row-major).
+ * G = H/128 groups per row, M = max_num_tokens, (e, s, g) = local expert,
+ * slot, group. */
+#define EP_SCALE_ROW_F32 0    /* fp32 [E_local, M, G] row-major: (e,s,g) at (e*M + s)*G + g */
+#define EP_SCALE_COL_F32 1    /* fp32 [E_local, M, G], last two dims column-major: (e,s,g) at (e*G + g)*M + s */
+#define EP_SCALE_COL_UE8M0 2  /* int32 [E_local, M, G/4], last two dims column-major: int (e,s,j) at
+                               * (e*(G/4) + j)*M + s; its byte i (least significant first) is the
+                               * UE8M0 code of group 4j+i.  Needs round_scale = 1 and H % 512 == 0. */
+
+/* [VB] BatchedPrepareAndFinalize.prepare, quantised branch, with the fp8
+ * payload of [UB] Buffer.low_latency_dispatch (use_fp8, round_scale,
+ * use_ue8m0): the slots, tokens_per_expert, capacity rule and slot handle of
+ * ep_batched_prepare, with rows of e4m3 codes b_q [E_local, M, H] and group
+ * scales b_scale in scale_fmt.  Each token is quantised once in 1x128 groups
+ * and every slot it takes carries the same bytes; with a = max(max|x|, 1e-4):
+ *   round_scale = 0: q = e4m3_rn_satfinite(x * (448/a)), scale = a/448 (fp32,
+ *     round to nearest even), exactly as ep_dispatch with fp8 = 1;
+ *   round_scale = 1: scale = the smallest power of two >= a/448 (the fp32
+ *     quotient), q = e4m3_rn_satfinite(x / scale) (exact division); its UE8M0
+ *     code is log2(scale) + 127.
+ * zero_pad != 0 zero-fills the codes and scale entries of slots at or past
+ * tokens_per_expert (the page's zero-initialised outputs); otherwise they are
+ * left untouched.  b_q 16-byte aligned, b_scale 4-byte aligned; ws as for
+ * ep_batched_prepare.
+ * Host errors: EP_ERR_UNSUPPORTED (H % 128 != 0; UE8M0 without round_scale or
+ * with H % 512 != 0), EP_ERR_INVALID_ARG (unknown scale_fmt, null pointers).
+ * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_TIMEOUT. */
+int ep_batched_prepare_fp8(const void *x, const int64_t *topk_idx, int64_t T, int K, int H,
+                           int E, int E_local, int rank, int max_num_tokens,
+                           uint8_t *b_q, void *b_scale, int scale_fmt, int round_scale,
+                           int32_t *tokens_per_expert, int32_t *slot, int zero_pad,
+                           void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
 /* [VB] BatchedPrepareAndFinalize.finalize, [UB] Buffer.low_latency_combine
  * ("reduce with weights"): this rank's partial
  *   out[t] = sum over k ascending with a local expert e_l = topk_idx[t,k] -

@@ -65,6 +65,17 @@ def test_argument_checks_reject_before_launch(lib):
                                ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
     assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 2, None, 0, None, None) == ep.EP_ERR_UNSUPPORTED  # dtype
     assert lib.ep_combine(None, 4, 64, None, 2, 4, None, 0, None, 0, None, None) == ep.EP_ERR_INVALID_ARG  # out
+    f = lib.ep_batched_prepare_fp8
+    f.argtypes = [vp, vp, ctypes.c_int64] + [ctypes.c_int] * 6 + [vp, vp, ctypes.c_int, ctypes.c_int, vp, vp,
+                                                                  ctypes.c_int, vp, ctypes.c_size_t, vp, vp]
+    args = lambda H, fmt, rs: (None, None, 4, 2, H, 8, 4, 0, 16, None, None, fmt, rs, None, None, 0, None, 0,
+                               None, None)
+    assert f(*args(512, 3, 1)) == ep.EP_ERR_INVALID_ARG          # unknown scale layout
+    assert f(*args(512, 0, 2)) == ep.EP_ERR_INVALID_ARG          # round_scale not 0/1
+    assert f(*args(192, 0, 0)) == ep.EP_ERR_UNSUPPORTED          # H % 128
+    assert f(*args(512, 2, 0)) == ep.EP_ERR_UNSUPPORTED          # UE8M0 needs round_scale
+    assert f(*args(384, 2, 1)) == ep.EP_ERR_UNSUPPORTED          # UE8M0 needs H % 512
+    assert f(*args(512, 1, 1)) == ep.EP_ERR_INVALID_ARG          # null outputs
 
 
 def test_no_entry_point_host_code_calls_exit(lib):

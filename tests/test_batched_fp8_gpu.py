@@ -1,0 +1,126 @@
+"""GPU parity of the fp8 expert-batched prepare (vLLM BatchedPrepareAndFinalize
+.prepare, quantised branch; NeMo uccl_ep.buffer Buffer.low_latency_dispatch
+scale formats) against the oracle: codes, scales in every layout, slots and
+tokens_per_expert bit for bit."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import combine_send_counts_gb300 as ep
+import oracle
+from combine_send_counts_gb300 import workloads as wl
+from _paths import assert_equal, np_, routing_inputs
+
+pytestmark = pytest.mark.gpu
+
+COMBOS = [(ep.EP_SCALE_ROW_F32, 0), (ep.EP_SCALE_COL_F32, 0), (ep.EP_SCALE_ROW_F32, 1), (ep.EP_SCALE_COL_F32, 1),
+          (ep.EP_SCALE_COL_UE8M0, 1)]
+
+
+def _wide_rows(T, H, seed):
+    """bf16 rows whose 128-groups span magnitudes 2^-120 .. 2^120 (plus an
+    all-zero group and a group at exactly 448)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    mag = 2.0 ** rng.integers(-120, 120, size=(T, H // 128, 1))
+    f = (rng.standard_normal((T, H // 128, 128)) * mag).astype(np.float32).reshape(T, H)
+    f[0, :128] = 0.0
+    if T > 1:
+        f[1, :128] = 448.0
+    bits = oracle.f32_to_bf16_bits(f).reshape(T, H)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def _compare(r, o, fmt, check_all=True):
+    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), o["tokens_per_expert"])
+    assert_equal("slot", np_(r["slot"]), o["slot"])
+    if check_all:
+        assert_equal("codes", np_(r["b_q"]), o["b_q"])
+        assert_equal("scales (bits)", np_(r["b_scale"]).view(np.uint32), o["b_scale"].view(np.uint32))
+        return
+    tpe = o["tokens_per_expert"]
+    for e in range(len(tpe)):
+        c = int(tpe[e])
+        assert_equal(f"codes e={e}", np_(r["b_q"][e, :c]), o["b_q"][e, :c])
+        gs = np_(r["b_scale"][e])
+        ws = o["b_scale"][e]
+        if fmt == ep.EP_SCALE_ROW_F32:
+            gs, ws = gs[:c], ws[:c]
+        else:
+            gs, ws = gs[:, :c], ws[:, :c]
+        assert_equal(f"scales e={e}", gs.view(np.uint32), ws.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt,rs", COMBOS)
+@pytest.mark.parametrize("zero_pad", [0, 1])
+def test_batched_fp8_small_all_layouts(fmt, rs, zero_pad):
+    T, H, K, E, El, rank, M = 1537, 1024, 6, 48, 12, 2, 300
+    idx, _ = routing_inputs(T, K, E, 31 + fmt, 0.15)
+    x = _wide_rows(T, H, 32)
+    o = oracle.batched_prepare_fp8(x, idx, E, El, rank, M, fmt, bool(rs), zero_pad=True)
+    r = ep.batched_prepare_fp8(x.cuda(), idx.cuda(), E, El, rank, M, fmt, bool(rs), zero_pad=bool(zero_pad))
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    _compare(r, o, fmt, check_all=bool(zero_pad))
+
+
+@pytest.mark.parametrize("fmt,rs", [(ep.EP_SCALE_COL_F32, 0), (ep.EP_SCALE_COL_UE8M0, 1)])
+def test_batched_fp8_workload_full_size(fmt, rs):
+    w = wl.WORKLOADS["batched"]
+    x, idx, _ = wl.make(w)
+    o = oracle.batched_prepare_fp8(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, fmt, bool(rs))
+    r = ep.batched_prepare_fp8(x.cuda(), idx.cuda(), w.E, w.E_local, w.rank, w.max_num_tokens, fmt, bool(rs))
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0 and o["err"] == 0
+    _compare(r, o, fmt, check_all=False)
+
+
+def test_batched_fp8_padding_left_untouched():
+    T, H, K, E, El, rank, M = 700, 512, 4, 16, 8, 1, 400
+    idx, _ = routing_inputs(T, K, E, 33, 0.0)
+    x = _wide_rows(T, H, 34)
+    dev = "cuda"
+    b_q = torch.full((El, M, H), 0xAB, dtype=torch.uint8, device=dev)
+    shape, dt = ep.batched_scale_storage(El, M, H, ep.EP_SCALE_COL_UE8M0)
+    b_s = torch.full(shape, 0x7F7F7F7F, dtype=dt, device=dev)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    err = ep.error_word()
+    ep.ep_batched_prepare_fp8(x.cuda(), idx.cuda(), T, K, H, E, El, rank, M, b_q, b_s, ep.EP_SCALE_COL_UE8M0, 1,
+                              tpe, slot, 0, ep.workspace(T, K, E // El, El), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o = oracle.batched_prepare_fp8(x, idx, E, El, rank, M, 2, True, False,
+                                   np.full((El, M, H), 0xAB, np.uint8), np.full(shape, 0x7F7F7F7F, np.int32))
+    assert_equal("codes incl. untouched padding", np_(b_q), o["b_q"])
+    assert_equal("packed scales incl. untouched padding", np_(b_s), o["b_scale"])
+
+
+def test_batched_fp8_capacity_overflow():
+    T, H, K, E, El, rank, M = 900, 256, 4, 8, 8, 0, 100
+    idx, _ = routing_inputs(T, K, E, 35, 0.0)
+    x = _wide_rows(T, H, 36)
+    o = oracle.batched_prepare_fp8(x, idx, E, El, rank, M, 1, False, zero_pad=True)
+    r = ep.batched_prepare_fp8(x.cuda(), idx.cuda(), E, El, rank, M, 1, False, zero_pad=True)
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) & ep.EP_ERR_CAPACITY and o["err"] & oracle.ERR_CAPACITY
+    _compare(r, o, 1)
+
+
+def test_batched_fp8_empty_and_host_checks():
+    dev = "cuda"
+    r = ep.batched_prepare_fp8(torch.empty((0, 512), dtype=torch.bfloat16, device=dev),
+                               torch.empty((0, 4), dtype=torch.int64, device=dev), 8, 4, 1, 16, 2, True,
+                               zero_pad=True)
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    assert int(r["tokens_per_expert"].abs().sum().item()) == 0
+    assert int(r["b_q"].abs().sum().item()) == 0 and int(r["b_scale"].abs().sum().item()) == 0
+    x = torch.zeros((4, 384), dtype=torch.bfloat16, device=dev)
+    idx = torch.zeros((4, 2), dtype=torch.int64, device=dev)
+    with pytest.raises(ep.EPError):
+        ep.batched_prepare_fp8(x, idx, 4, 4, 0, 8, ep.EP_SCALE_COL_UE8M0, True)    # H % 512
+    with pytest.raises(ep.EPError):
+        ep.batched_prepare_fp8(torch.zeros((4, 512), dtype=torch.bfloat16, device=dev), idx, 4, 4, 0, 8,
+                               ep.EP_SCALE_COL_UE8M0, False)                                 # no round_scale
