@@ -69,6 +69,10 @@ def _load():
         "orc_batched_combine": (None, [P, P, P, P, i64, i32, i32, i32, i32, i32, P]),
         "orc_quantize_fp8_rows_pow2": (None, [P, i64, i32, P, P, P]),
         "orc_batched_prepare_fp8": (i32, [P, P, i64, i32, i32, i32, i32, i32, i32, P, P, i32, i32, P, P, i32]),
+        "orc_expert_capacity": (i64, [i64, i32, i32, ctypes.c_double]),
+        "orc_batched_prepare_ex": (i32, [P, P, i64, i32, i32, i32, i32, i32, i32, i32, i32, P, P, i32, i32, P, P,
+                                         P, i32]),
+        "orc_align_send_layout": (i64, [P, i32, i32, i32, i64, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -227,6 +231,63 @@ def batched_prepare_fp8(x, topk_idx, E: int, E_local: int, rank: int, M: int, fm
                                           _ptr(b_s), int(fmt), int(round_scale), _ptr(tpe), _ptr(slot),
                                           int(zero_pad))
     return dict(b_q=b_q, b_scale=b_s, tokens_per_expert=tpe, slot=slot, err=int(err))
+
+
+def expert_capacity(T: int, K: int, E: int, factor: float) -> int:
+    return int(_load().orc_expert_capacity(T, K, E, float(factor)))
+
+
+def batched_prepare_ex(x, topk_idx, E: int, E_local: int, rank: int, M: int, capacity: Optional[int] = None,
+                       alignment: int = 1, fmt: Optional[int] = None, round_scale: bool = False,
+                       zero_pad: bool = False, rows_init=None, scale_init=None):
+    """Expert-batched prepare with a per-expert capacity and receive alignment.
+    fmt None: bf16 rows (uint16 bits); else fp8 codes + scales in layout fmt.
+    -> dict(b_rows, b_scale (or None), tokens_per_expert, slot, dropped, err)."""
+    xb = _bf16_bits(x)
+    idx = _c(topk_idx, np.int64)
+    T, H = xb.shape
+    K = idx.shape[1]
+    C = M if capacity is None else int(capacity)
+    if fmt is None:
+        rows = np.zeros((E_local, M, H), np.uint16) if rows_init is None else np.array(rows_init, np.uint16)
+        b_s = None
+    else:
+        rows = np.zeros((E_local, M, H), np.uint8) if rows_init is None else np.array(rows_init, np.uint8)
+        shape, dt = batched_scale_shape(E_local, M, H, fmt)
+        b_s = np.zeros(shape, dt) if scale_init is None else np.array(scale_init, dt)
+    tpe = np.empty(E_local, np.int32)
+    slot = np.empty((T, K), np.int32)
+    dropped = np.empty(E_local, np.int32)
+    err = _load().orc_batched_prepare_ex(_ptr(xb), _ptr(idx), T, K, H, E, E_local, rank, M, C, int(alignment),
+                                         _ptr(rows), _ptr(b_s), -1 if fmt is None else int(fmt),
+                                         int(round_scale), _ptr(tpe), _ptr(slot), _ptr(dropped), int(zero_pad))
+    return dict(b_rows=rows, b_scale=b_s, tokens_per_expert=tpe, slot=slot, dropped=dropped, err=int(err))
+
+
+def align_send_layout(layout: dict, send_counts, A: int) -> dict:
+    """The send layout with every rank's segment padded to a multiple of A rows
+    (pad rows: token -1, rank p, no experts); plus the aligned rank_offsets."""
+    sc = _c(send_counts, np.int32)
+    P = sc.shape[0]
+    sti = _c(layout["send_token_idx"], np.int32)
+    si = _c(layout["send_idx"], np.int64)
+    sw = _c(layout["send_w"], np.float32)
+    tp = _c(layout["token_pos"], np.int32)
+    T = tp.shape[0]
+    K = si.shape[1] if si.ndim == 2 else 1
+    n = int(sum(-(-int(c) // A) * A for c in sc))
+    ro = np.empty(P + 1, np.int32)
+    a_ti = np.empty(max(n, 1), np.int32)
+    a_r = np.empty(max(n, 1), np.int32)
+    a_i = np.empty((max(n, 1), K), np.int64)
+    a_w = np.empty((max(n, 1), K), np.float32)
+    a_tp = np.empty((T, P), np.int32)
+    got = _load().orc_align_send_layout(_ptr(sc), P, A, K, T, _ptr(sti), _ptr(si.reshape(-1, K)),
+                                        _ptr(sw.reshape(-1, K)), _ptr(tp), _ptr(ro), _ptr(a_ti), _ptr(a_r),
+                                        _ptr(a_i), _ptr(a_w), _ptr(a_tp))
+    assert got == n
+    return dict(n=n, rank_offsets=ro, send_token_idx=a_ti[:n], send_rank=a_r[:n], send_idx=a_i[:n],
+                send_w=a_w[:n], token_pos=a_tp)
 
 
 def dispatch_fp8(x, send_token_idx):

@@ -21,7 +21,8 @@
  *         BatchedPrepareAndFinalize.prepare (hit mask, tokens_per_expert,
  *         slots that preserve token order) and .finalize.
  *   [ND]  NeMo AutoModel docs, ...moe.megatron.token_dispatcher:
- *         TokenDispatcherConfig.moe_router_dtype (weighting in fp32).
+ *         TokenDispatcherConfig.moe_router_dtype (weighting in fp32),
+ *         moe_expert_capacity_factor, moe_router_expert_pad_multiple.
  *   bfloat16: the upper half of an IEEE-754 binary32.
  *   E4M3: OCP 8-bit Floating Point Specification (OFP8) v1.0, E4M3 format
  *         (bias 7, no infinities, S.1111.111 is NaN, max finite 448).
@@ -44,7 +45,14 @@
  *   - power-of-two scales (round_scale): the smallest power of two >= a/448,
  *     so x / scale never exceeds 448; the UE8M0 code is its biased exponent;
  *     four codes pack into an int32 with group 4j+i at byte i (least
- *     significant first).
+ *     significant first);
+ *   - capacity: an expert keeps its first `capacity` tokens in token order,
+ *     later ones are dropped and counted (no error bit); capacity from a
+ *     factor is ceil(factor * T * K / E);
+ *   - alignment: the kept per-expert count is rounded up to the alignment
+ *     (at most M) and the rows in between are zero rows; on the send layout
+ *     every rank segment is padded to a multiple of the alignment with rows
+ *     that carry no token.
  *
  * Build: plain C11, -O2 -fno-fast-math -ffp-contract=off (no contraction of
  * a*b+c, so every rounding is the one written here).
@@ -582,4 +590,167 @@ int orc_batched_prepare_fp8(const uint16_t *x, const int64_t *topk_idx, int64_t 
     free(sc);
     free(code);
     return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [VB] prepare (both branches) with a per-expert capacity and a receive      */
+/* alignment ([ND] TokenDispatcherConfig moe_expert_capacity_factor: "the     */
+/* capacity factor for each expert, None means no token will be dropped";     */
+/* [UB] Buffer.dispatch expert_alignment: "align the number of tokens         */
+/* received by each local expert"; [ND] moe_router_expert_pad_multiple).      */
+/* Local expert e_l keeps the first `capacity` tokens naming it, in token     */
+/* order (slots 0 .. capacity-1); later ones are dropped (slot -1, row not    */
+/* written) and counted in dropped[e_l]; this is the capacity's purpose, so   */
+/* no error bit.  The received count kept = min(hits, capacity) is rounded    */
+/* up to a multiple of `alignment` (at most M) and returned as               */
+/* tokens_per_expert; rows kept .. aligned-1 are zero rows (codes 0 and zero */
+/* scale entries for fp8), rows past that are zeroed only with zero_pad.      */
+/* fmt < 0: bf16 rows (b_rows is uint16 [E_local,M,H]); fmt 0..2: fp8 codes   */
+/* (b_rows is uint8) with scales as orc_batched_prepare_fp8.                  */
+/* Returns error bits (invalid ids 2; 16 for an unsupported fp8 format).     */
+/* ------------------------------------------------------------------------ */
+int64_t orc_expert_capacity(int64_t T, int K, int E, double factor)
+{
+    return (int64_t)ceil(factor * (double)T * (double)K / (double)E);
+}
+
+int orc_batched_prepare_ex(const uint16_t *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
+                           int E_local, int rank, int M, int capacity, int alignment, void *b_rows,
+                           void *b_scale, int fmt, int round_scale, int32_t *tokens_per_expert,
+                           int32_t *slot, int32_t *dropped, int zero_pad)
+{
+    int G = H / 128;
+    if (fmt >= 0 && (H % 128 != 0 || (fmt == 2 && (!round_scale || H % 512 != 0))))
+        return 16;
+    size_t rowb = fmt < 0 ? (size_t)H * 2 : (size_t)H;   /* bytes per row */
+    uint8_t *rows = (uint8_t *)b_rows;
+    uint8_t *q = NULL, *code = NULL;
+    float *sc = NULL;
+    if (fmt >= 0) {
+        q = (uint8_t *)malloc((size_t)(T > 0 ? T : 1) * H);
+        sc = (float *)malloc((size_t)(T > 0 ? T : 1) * G * sizeof(float));
+        code = (uint8_t *)malloc((size_t)(T > 0 ? T : 1) * G);
+        if (round_scale)
+            orc_quantize_fp8_rows_pow2(x, T, H, q, sc, code);
+        else
+            orc_quantize_fp8_rows(x, T, H, q, sc);
+    }
+    float *sf = (float *)b_scale;
+    uint8_t *sb = (uint8_t *)b_scale;
+    int err = 0;
+    for (int64_t i = 0; i < T * K; ++i) {
+        slot[i] = -1;
+        int64_t id = topk_idx[i];
+        if (id < -1 || id >= E)
+            err |= ORC_ERR_INVALID_EXPERT;
+    }
+    for (int el = 0; el < E_local; ++el) {
+        int64_t e = (int64_t)rank * E_local + el;
+        int64_t s = 0;
+        for (int64_t t = 0; t < T; ++t) {
+            int hit = 0;
+            for (int k = 0; k < K; ++k)
+                if (topk_idx[t * K + k] == e)
+                    hit = 1;
+            if (!hit)
+                continue;
+            if (s < capacity) {
+                uint8_t *dst = rows + ((int64_t)el * M + s) * rowb;
+                if (fmt < 0)
+                    memcpy(dst, x + t * H, rowb);
+                else {
+                    memcpy(dst, q + t * H, rowb);
+                    for (int g = 0; g < G; ++g) {
+                        if (fmt == 0)
+                            sf[((int64_t)el * M + s) * G + g] = sc[t * G + g];
+                        else if (fmt == 1)
+                            sf[((int64_t)el * G + g) * M + s] = sc[t * G + g];
+                        else
+                            sb[(((int64_t)el * (G / 4) + g / 4) * M + s) * 4 + g % 4] = code[t * G + g];
+                    }
+                }
+                for (int k = 0; k < K; ++k)
+                    if (topk_idx[t * K + k] == e)
+                        slot[t * K + k] = (int32_t)s;
+            }
+            ++s;
+        }
+        int64_t kept = s < capacity ? s : capacity;
+        int64_t aligned = (kept + alignment - 1) / alignment * alignment;
+        if (aligned > M)
+            aligned = M;
+        tokens_per_expert[el] = (int32_t)aligned;
+        if (dropped)
+            dropped[el] = (int32_t)(s - kept);
+        int64_t zero_end = zero_pad ? M : aligned;
+        for (int64_t r = kept; r < zero_end; ++r) {
+            memset(rows + ((int64_t)el * M + r) * rowb, 0, rowb);
+            for (int g = 0; fmt >= 0 && g < G; ++g) {
+                if (fmt == 0)
+                    sf[((int64_t)el * M + r) * G + g] = 0.0f;
+                else if (fmt == 1)
+                    sf[((int64_t)el * G + g) * M + r] = 0.0f;
+                else
+                    sb[(((int64_t)el * (G / 4) + g / 4) * M + r) * 4 + g % 4] = 0;
+            }
+        }
+    }
+    free(q);
+    free(sc);
+    free(code);
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* expert_alignment on the send layout ([UB] Buffer.dispatch): every rank's   */
+/* segment of the rank-major send buffer starts at a multiple of A rows;     */
+/* rank p's rows keep their order, followed by round_up(count_p, A) -        */
+/* count_p pad rows that carry no token (send_token_idx -1, send_rank p,     */
+/* send_idx -1, send_w +0).  token_pos points at the moved rows.  Input: the  */
+/* unaligned layout of orc_build_send_layout and its send_counts.  Output    */
+/* arrays hold round-up sizes; returns the aligned row count.                */
+/* ------------------------------------------------------------------------ */
+int64_t orc_align_send_layout(const int32_t *send_counts, int P, int A, int K, int64_t T,
+                              const int32_t *send_token_idx, const int64_t *send_idx, const float *send_w,
+                              const int32_t *token_pos, int32_t *rank_offsets, int32_t *a_token_idx,
+                              int32_t *a_rank, int64_t *a_idx, float *a_w, int32_t *a_token_pos)
+{
+    int64_t src = 0, dst = 0;
+    for (int p = 0; p < P; ++p) {
+        rank_offsets[p] = (int32_t)dst;
+        int64_t c = send_counts[p];
+        int64_t padded = (c + A - 1) / A * A;
+        for (int64_t i = 0; i < padded; ++i, ++dst) {
+            if (i < c) {
+                a_token_idx[dst] = send_token_idx[src + i];
+                a_rank[dst] = p;
+                for (int k = 0; k < K; ++k) {
+                    a_idx[dst * K + k] = send_idx[(src + i) * K + k];
+                    a_w[dst * K + k] = send_w[(src + i) * K + k];
+                }
+            } else {
+                a_token_idx[dst] = -1;
+                a_rank[dst] = p;
+                for (int k = 0; k < K; ++k) {
+                    a_idx[dst * K + k] = -1;
+                    a_w[dst * K + k] = 0.0f;
+                }
+            }
+        }
+        src += c;
+    }
+    rank_offsets[P] = (int32_t)dst;
+    for (int64_t t = 0; t < T; ++t)
+        for (int p = 0; p < P; ++p) {
+            int64_t n = token_pos[t * P + p];
+            a_token_pos[t * P + p] = -1;
+            if (n < 0)
+                continue;
+            /* row n of rank p moves by the padding of the ranks before p */
+            int64_t pad = 0;
+            for (int q2 = 0; q2 < p; ++q2)
+                pad += (send_counts[q2] + A - 1) / A * A - send_counts[q2];
+            a_token_pos[t * P + p] = (int32_t)(n + pad);
+        }
+    return dst;
 }
