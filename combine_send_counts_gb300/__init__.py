@@ -76,6 +76,9 @@ _SIGNATURES = {
                                                 _VP]),
     "ep_batched_prepare_fp8": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _I32, _I32,
                                       _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
+    "ep_batched_prepare_ex": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP,
+                                     _I32, _I32, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
+    "ep_expert_capacity": (_I64, [_I64, _I32, _I32, ctypes.c_double]),
 }
 
 EP_SCALE_ROW_F32, EP_SCALE_COL_F32, EP_SCALE_COL_UE8M0 = 0, 1, 2
@@ -468,6 +471,57 @@ def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank:
     ep_batched_prepare(x, topk_idx, T, K, H, num_experts, El, rank, max_num_tokens, b_x, tpe, slot,
                        int(zero_pad), ws, err, stream)
     return dict(b_x=b_x, tokens_per_expert=tpe, slot=slot, err=err)
+
+
+def ep_batched_prepare_ex(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, capacity, alignment, b_rows,
+                          b_scale, scale_fmt, round_scale, tokens_per_expert, slot, dropped, zero_pad, ws, err,
+                          stream=None):
+    rc = load().ep_batched_prepare_ex(_p(x), _p(topk_idx), int(T), int(K), int(H), int(E), int(E_local), int(rank),
+                                      int(max_num_tokens), int(capacity), int(alignment), _p(b_rows), _p(b_scale),
+                                      int(scale_fmt), int(round_scale), _p(tokens_per_expert), _p(slot),
+                                      _p(dropped), int(zero_pad), _p(ws), ws.numel() * ws.element_size(), _p(err),
+                                      _stream(stream))
+    _check(rc, "ep_batched_prepare_ex")
+
+
+def ep_expert_capacity(T: int, K: int, E: int, factor: float) -> int:
+    v = int(load().ep_expert_capacity(int(T), int(K), int(E), float(factor)))
+    if v < 0:
+        raise EPError(EP_ERR_INVALID_ARG, "ep_expert_capacity")
+    return v
+
+
+def expert_capacity(num_tokens: int, topk: int, num_experts: int, capacity_factor: float) -> int:
+    """Tokens each expert keeps under a capacity factor: ceil(factor * T * K / E)."""
+    return ep_expert_capacity(num_tokens, topk, num_experts, capacity_factor)
+
+
+def batched_prepare_ex(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int, *,
+                       capacity: int = 0, alignment: int = 1, scale_fmt: Optional[int] = None,
+                       round_scale: bool = False, zero_pad: bool = False, err=None, stream=None):
+    """Expert-batched prepare with a per-expert capacity (0: max_num_tokens,
+    overflow is an error; else later tokens are dropped and counted) and a
+    receive alignment.  scale_fmt None: bf16 rows; else fp8 codes + scales.
+    -> dict(b_rows, b_scale, tokens_per_expert, slot, dropped, err)."""
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    El, M = num_local_experts, max_num_tokens
+    dev = x.device
+    fp8 = scale_fmt is not None
+    b_rows = torch.empty((El, M, H), dtype=torch.uint8 if fp8 else x.dtype, device=dev)
+    b_s = None
+    if fp8:
+        shape, dt = batched_scale_storage(El, M, H, scale_fmt)
+        b_s = torch.empty(shape, dtype=dt, device=dev)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    dropped = torch.empty(El, dtype=torch.int32, device=dev)
+    ws = workspace(T, K, num_experts // El, El, 1, dev)
+    err = err if err is not None else error_word(dev)
+    ep_batched_prepare_ex(x, topk_idx, T, K, H, num_experts, El, rank, M, capacity, alignment, b_rows, b_s,
+                          -1 if not fp8 else scale_fmt, int(round_scale), tpe, slot, dropped, int(zero_pad), ws,
+                          err, stream)
+    return dict(b_rows=b_rows, b_scale=b_s, tokens_per_expert=tpe, slot=slot, dropped=dropped, err=err)
 
 
 def batched_scale_storage(E_local: int, M: int, H: int, scale_fmt: int):

@@ -1,10 +1,10 @@
 // Combine kernels of libep_gb300:
 //   ep_combine          -- axolotl integrations.expert_parallel.torch_dispatch,
 //                          combine; NeMo uccl_ep.buffer, Buffer.combine
-//                          (addition without weights)
+//                          (an unweighted sum)
 //   ep_batched_combine  -- vLLM BatchedPrepareAndFinalize.finalize; NeMo
 //                          uccl_ep.buffer, Buffer.low_latency_combine (reduce
-//                          with weights)
+//                          weighted)
 //
 // Both read, for every output token, its source rows in a fixed order and
 // accumulate them in fp32.  The work is HBM-bound and its rows are scattered,

@@ -37,9 +37,20 @@ struct ChunkTable {
     int64_t start[EP_MAX_CHUNKS + 1];
 };
 
+// Per-expert slot limits of the expert-batched layout.
+struct SlotLimits {
+    int M;              // rows per expert in the layout
+    int cap;            // slots kept per expert (<= M); later tokens are dropped
+    int silent;         // drops past cap are the capacity's purpose (no error bit)
+    int align;          // tokens_per_expert = min(round_up(kept, align), M)
+    int32_t *dropped;   // [E_local] tokens dropped per expert, or null
+    int32_t *kept;      // [E_local] tokens kept per expert, or null
+};
+
 // Launchers implemented in ep_route.cu and used by the batched entry points.
+// The workspace [ws, ws + ws_bytes) is theirs.
 int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
-                         int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
+                         const SlotLimits &lim, int32_t *tokens_per_expert, int32_t *slot,
                          void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream);
 
 // The synthetic fp8 expert over N rows (ep_move.cu); with n_rows non-NULL,

@@ -228,32 +228,34 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
 }
 
 // ------------------------------------------------------------- zero padding --
-// Zero rows [tokens_per_expert[e], M) of every local expert (16-byte stores).
-__global__ void zero_pad_kernel(uint4 *__restrict__ b_x, const int32_t *__restrict__ tokens_per_expert,
-                                int M, int nvec)
+// Zero rows [first[e], end) of every local expert, end = M when full, else
+// tokens_per_expert[e] (the aligned count); 16-byte stores.
+__global__ void zero_rows_kernel(uint4 *__restrict__ b_x, const int32_t *__restrict__ first,
+                                 const int32_t *__restrict__ tokens_per_expert, int full, int M, int nvec)
 {
     const int e = blockIdx.y;
-    const int64_t first = (int64_t)tokens_per_expert[e] * nvec;
-    const int64_t total = (int64_t)M * nvec;
-    uint4 *base = b_x + (int64_t)e * total;
+    const int64_t lo = (int64_t)first[e] * nvec;
+    const int64_t hi = (int64_t)(full ? M : tokens_per_expert[e]) * nvec;
+    uint4 *base = b_x + (int64_t)e * M * nvec;
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int64_t i = first + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x)
+    for (int64_t i = lo + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi; i += (int64_t)gridDim.x * blockDim.x)
         st_stream(base + i, z);
 }
 
-// Zero the scale entries of slots [tokens_per_expert[e], M) of every local
-// expert, in any scale layout (4-byte entries; UE8M0 ints hold 4 groups).
-__global__ void zero_pad_scales_kernel(ScaleSpec sp, const int32_t *__restrict__ tokens_per_expert, int groups)
+// Zero the scale entries of slots [first[e], end) of every local expert (end
+// as zero_rows_kernel), in any scale layout (4-byte entries; UE8M0 ints hold
+// 4 groups of one slot).
+__global__ void zero_scales_kernel(ScaleSpec sp, const int32_t *__restrict__ first,
+                                   const int32_t *__restrict__ tokens_per_expert, int full, int groups)
 {
     const int e = blockIdx.y;
-    const int first = tokens_per_expert[e];
+    const int lo = first[e], hi = full ? sp.M : tokens_per_expert[e];
     const int per_row = sp.fmt == EP_SCALE_COL_UE8M0 ? groups / 4 : groups;
     const int64_t total = (int64_t)sp.M * per_row;
     uint32_t *base = static_cast<uint32_t *>(sp.out) + (int64_t)e * total;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t s = sp.fmt == EP_SCALE_ROW_F32 ? i / per_row : i % sp.M;
-        if (s >= first)
+        if (s >= lo && s < hi)
             base[i] = 0u;
     }
 }
@@ -485,55 +487,102 @@ extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token
     return launch_scatter_bf16(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, err, stream);
 }
 
-// bf16 rows (sp == nullptr) or fp8 codes with scales as *sp.
+// bf16 rows (sp == nullptr) or fp8 codes with scales as *sp; capacity 0
+// means M with overflow reported, 1..M drops silently past it.
 static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E, int E_local,
-                           int rank, int max_num_tokens, void *b_x, const ScaleSpec *sp,
-                           int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws, size_t ws_bytes,
-                           int32_t *err, cudaStream_t stream)
+                           int rank, int M, int capacity, int alignment, void *b_x, const ScaleSpec *sp,
+                           int32_t *tokens_per_expert, int32_t *slot, int32_t *dropped, int zero_pad, void *ws,
+                           size_t ws_bytes, int32_t *err, cudaStream_t stream)
 {
     if (!row_shape_ok(T, H) || K < 1 || K > EP_MAX_TOPK || E_local < 1 || E < E_local || E % E_local != 0)
         return EP_ERR_INVALID_ARG;
-    if (rank < 0 || (int64_t)(rank + 1) * E_local > E || max_num_tokens < 0)
+    if (rank < 0 || (int64_t)(rank + 1) * E_local > E || M < 0)
         return EP_ERR_INVALID_ARG;
-    if ((int64_t)E_local * max_num_tokens >= ((int64_t)1 << 31))
+    if (capacity < 0 || capacity > M || alignment < 1)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)E_local * M >= ((int64_t)1 << 31))
         return EP_ERR_UNSUPPORTED;
     if (tokens_per_expert == nullptr || ws == nullptr || !aligned(ws, kWsAlign))
         return EP_ERR_INVALID_ARG;
     if (T > 0 && (x == nullptr || topk_idx == nullptr || slot == nullptr || !aligned(x, 16)))
         return EP_ERR_INVALID_ARG;
-    if ((int64_t)E_local * max_num_tokens > 0 &&
+    if ((int64_t)E_local * M > 0 &&
         (b_x == nullptr || !aligned(b_x, 16) || (sp != nullptr && (sp->out == nullptr || !aligned(sp->out, 4)))))
         return EP_ERR_INVALID_ARG;
-    if (ws_bytes < kWsAlign + (size_t)ceil_div(T, kRouteThreads) * E_local * sizeof(int32_t))
+    // the kept counts live at the end of the workspace; the slot launchers
+    // take what is before them
+    const size_t kept_bytes = align_up((size_t)E_local * sizeof(int32_t), kWsAlign);
+    if (ws_bytes < kWsAlign + (size_t)ceil_div(T, kRouteThreads) * E_local * sizeof(int32_t) + kept_bytes)
         return EP_ERR_INVALID_ARG;
+    const size_t slot_ws = (ws_bytes - kept_bytes) / kWsAlign * kWsAlign;
+    int32_t *kept = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + slot_ws);
 
-    int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, max_num_tokens, tokens_per_expert,
-                                  slot, ws, ws_bytes, err, stream);
+    const SlotLimits lim{M, capacity > 0 ? capacity : M, capacity > 0, alignment, dropped, kept};
+    int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, lim, tokens_per_expert, slot, ws, slot_ws,
+                                  err, stream);
     if (rc != EP_OK)
         return rc;
     if (T > 0) {
-        const BatchedRows rows{topk_idx, slot, nullptr, K, (int64_t)rank * E_local, E_local, max_num_tokens, true};
-        const int64_t n_rows = (int64_t)E_local * max_num_tokens;
+        const BatchedRows rows{topk_idx, slot, nullptr, K, (int64_t)rank * E_local, E_local, M, true};
+        const int64_t n_rows = (int64_t)E_local * M;
         rc = sp == nullptr ? launch_scatter_bf16(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, err, stream)
                            : launch_scatter_fp8(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, *sp, err, stream);
         if (rc != EP_OK)
             return rc;
     }
-    if (zero_pad && max_num_tokens > 0) {
+    // zero rows: the alignment rows [kept, aligned) always, the rest with zero_pad
+    if ((zero_pad || alignment > 1) && M > 0) {
         const int nvec = sp == nullptr ? H / 8 : H / 16;   // 16-byte vectors per row
-        dim3 grid((unsigned)std::min<int64_t>(ceil_div((int64_t)max_num_tokens * nvec, 256), 1024), E_local);
-        zero_pad_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), tokens_per_expert, max_num_tokens,
-                                                  nvec);
+        dim3 grid((unsigned)std::min<int64_t>(ceil_div((int64_t)M * nvec, 256), 1024), E_local);
+        zero_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), kept, tokens_per_expert, zero_pad, M,
+                                                   nvec);
         if ((rc = launch_status()) != EP_OK)
             return rc;
         if (sp != nullptr) {
-            dim3 sgrid((unsigned)std::min<int64_t>(ceil_div((int64_t)max_num_tokens * (H / 128), 256), 256),
-                       E_local);
-            zero_pad_scales_kernel<<<sgrid, 256, 0, stream>>>(*sp, tokens_per_expert, H / 128);
+            dim3 sgrid((unsigned)std::min<int64_t>(ceil_div((int64_t)M * (H / 128), 256), 256), E_local);
+            zero_scales_kernel<<<sgrid, 256, 0, stream>>>(*sp, kept, tokens_per_expert, zero_pad, H / 128);
             return launch_status();
         }
     }
     return EP_OK;
+}
+
+static int scale_spec(int scale_fmt, int round_scale, int H, void *b_scale, int M, ScaleSpec *sp)
+{
+    if (scale_fmt != EP_SCALE_ROW_F32 && scale_fmt != EP_SCALE_COL_F32 && scale_fmt != EP_SCALE_COL_UE8M0)
+        return EP_ERR_INVALID_ARG;
+    if (round_scale != 0 && round_scale != 1)
+        return EP_ERR_INVALID_ARG;
+    if (H % 128 != 0 || (scale_fmt == EP_SCALE_COL_UE8M0 && (!round_scale || H % 512 != 0)))
+        return EP_ERR_UNSUPPORTED;
+    *sp = ScaleSpec{b_scale, scale_fmt, round_scale, M};
+    return EP_OK;
+}
+
+extern "C" int ep_batched_prepare_ex(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
+                                     int E_local, int rank, int max_num_tokens, int capacity, int alignment,
+                                     void *b_rows, void *b_scale, int scale_fmt, int round_scale,
+                                     int32_t *tokens_per_expert, int32_t *slot, int32_t *dropped, int zero_pad,
+                                     void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream)
+{
+    ScaleSpec sp{};
+    if (scale_fmt >= 0) {
+        const int rc = scale_spec(scale_fmt, round_scale, H, b_scale, max_num_tokens, &sp);
+        if (rc != EP_OK)
+            return rc;
+    } else if (scale_fmt != -1) {
+        return EP_ERR_INVALID_ARG;
+    }
+    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, capacity, alignment, b_rows,
+                           scale_fmt >= 0 ? &sp : nullptr, tokens_per_expert, slot, dropped, zero_pad, ws, ws_bytes,
+                           err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int64_t ep_expert_capacity(int64_t T, int K, int E, double factor)
+{
+    if (T < 0 || K < 1 || E < 1 || !(factor > 0.0))
+        return -1;
+    return (int64_t)ceil(factor * (double)T * (double)K / (double)E);
 }
 
 extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H, int E,
@@ -541,8 +590,8 @@ extern "C" int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_
                                   int32_t *tokens_per_expert, int32_t *slot, int zero_pad, void *ws,
                                   size_t ws_bytes, int32_t *err, ep_stream_t stream)
 {
-    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b_x, nullptr,
-                           tokens_per_expert, slot, zero_pad, ws, ws_bytes, err,
+    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, 0, 1, b_x, nullptr,
+                           tokens_per_expert, slot, nullptr, zero_pad, ws, ws_bytes, err,
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -551,15 +600,13 @@ extern "C" int ep_batched_prepare_fp8(const void *x, const int64_t *topk_idx, in
                                       int scale_fmt, int round_scale, int32_t *tokens_per_expert, int32_t *slot,
                                       int zero_pad, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream)
 {
-    if (scale_fmt != EP_SCALE_ROW_F32 && scale_fmt != EP_SCALE_COL_F32 && scale_fmt != EP_SCALE_COL_UE8M0)
-        return EP_ERR_INVALID_ARG;
-    if (round_scale != 0 && round_scale != 1)
-        return EP_ERR_INVALID_ARG;
-    if (H % 128 != 0 || (scale_fmt == EP_SCALE_COL_UE8M0 && (!round_scale || H % 512 != 0)))
-        return EP_ERR_UNSUPPORTED;
-    const ScaleSpec sp{b_scale, scale_fmt, round_scale, max_num_tokens};
-    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, b_q, &sp, tokens_per_expert,
-                           slot, zero_pad, ws, ws_bytes, err, reinterpret_cast<cudaStream_t>(stream));
+    ScaleSpec sp{};
+    const int rc = scale_spec(scale_fmt, round_scale, H, b_scale, max_num_tokens, &sp);
+    if (rc != EP_OK)
+        return rc;
+    return batched_prepare(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens, 0, 1, b_q, &sp,
+                           tokens_per_expert, slot, nullptr, zero_pad, ws, ws_bytes, err,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 namespace ep {

@@ -502,8 +502,20 @@ batched_count_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E, i
     raise(err, bad);
 }
 
+// Block 0's per-expert totals: kept count, aligned tokens_per_expert, drops.
+__device__ __forceinline__ int finish_expert_count(const SlotLimits &L, int e, int tot, int32_t *tokens_per_expert)
+{
+    const int kept = min(tot, L.cap);
+    tokens_per_expert[e] = min((kept + L.align - 1) / L.align * L.align, L.M);
+    if (L.dropped != nullptr)
+        L.dropped[e] = tot - kept;
+    if (L.kept != nullptr)
+        L.kept[e] = kept;
+    return tot > L.cap && !L.silent ? EP_ERR_CAPACITY : 0;
+}
+
 __global__ void __launch_bounds__(kRouteThreads)
-batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_local, int64_t e0, int M,
+batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_local, int64_t e0, SlotLimits lim,
                     const int32_t *__restrict__ part, int nb, int32_t *__restrict__ tokens_per_expert,
                     int32_t *__restrict__ slot, int32_t *err)
 {
@@ -532,12 +544,8 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
                 atomicAdd(&s_base[e], v);
         }
         __syncthreads();
-        if (blockIdx.x == 0 && threadIdx.x < ng) {
-            const int tot = s_tot[threadIdx.x];
-            tokens_per_expert[g0 + threadIdx.x] = min(tot, M);
-            if (tot > M)
-                bad = EP_ERR_CAPACITY;
-        }
+        if (blockIdx.x == 0 && threadIdx.x < ng)
+            bad |= finish_expert_count(lim, g0 + threadIdx.x, s_tot[threadIdx.x], tokens_per_expert);
         const uint64_t mask = valid ? local_mask(idx + t * K, K, e0 + g0, ng) : 0;
         for (int e = 0; e < ng; ++e) {
             const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
@@ -559,8 +567,8 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
             if (!valid || !((mask >> e) & 1ull))
                 continue;
             const int s = s_base[e] + s_warp[warp][e] + __popc(bal & lanemask_lt());
-            const int32_t v = s < M ? s : -1;
-            if (s >= M)
+            const int32_t v = s < lim.cap ? s : -1;
+            if (s >= lim.cap && !lim.silent)
                 bad = EP_ERR_CAPACITY;
             for (int k = 0; k < K; ++k)
                 if (idx[t * K + k] == e0 + g0 + e)
@@ -934,7 +942,7 @@ struct BatchedFusedArgs {
     int64_t T;
     int K, E, E_local;
     int64_t e0;
-    int M;
+    SlotLimits lim;
     int32_t *tokens_per_expert;
     int32_t *slot;
     int32_t *part;                    // [gridDim][E_local]
@@ -1010,12 +1018,8 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
     __syncthreads();
     block_rank_sums(a.part, nb, El, b, s_tot, s_before);
     __syncthreads();
-    if (b == 0 && threadIdx.x < El) {
-        const int tot = s_tot[threadIdx.x];
-        a.tokens_per_expert[threadIdx.x] = min(tot, a.M);
-        if (tot > a.M)
-            bad = EP_ERR_CAPACITY;
-    }
+    if (b == 0 && threadIdx.x < El)
+        bad |= finish_expert_count(a.lim, threadIdx.x, s_tot[threadIdx.x], a.tokens_per_expert);
     int32_t sl[KM];
 #pragma unroll
     for (int k = 0; k < KM; ++k)
@@ -1025,8 +1029,8 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
         if (!((mask >> e) & 1ull))
             continue;
         const int s = s_before[e] + s_warp[warp][e] + __popc(bal & lanemask_lt());
-        const int v = s < a.M ? s : -1;
-        if (s >= a.M)
+        const int v = s < a.lim.cap ? s : -1;
+        if (s >= a.lim.cap && !a.lim.silent)
             bad = EP_ERR_CAPACITY;
 #pragma unroll
         for (int k = 0; k < KM; ++k)
@@ -1074,13 +1078,14 @@ static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t 
 }
 
 int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
-                         int max_num_tokens, int32_t *tokens_per_expert, int32_t *slot,
+                         const SlotLimits &lim, int32_t *tokens_per_expert, int32_t *slot,
                          void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream)
 {
     const int64_t e0 = (int64_t)rank * E_local;
     if (T == 0) {   // every expert receives nothing
-        if (cudaMemsetAsync(tokens_per_expert, 0, sizeof(int32_t) * E_local, stream) != cudaSuccess)
-            return EP_ERR_CUDA;
+        for (int32_t *p : {tokens_per_expert, lim.dropped, lim.kept})
+            if (p != nullptr && cudaMemsetAsync(p, 0, sizeof(int32_t) * E_local, stream) != cudaSuccess)
+                return EP_ERR_CUDA;
         return EP_OK;
     }
     // one cooperative launch when the local experts fit one mask word, the
@@ -1090,7 +1095,7 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
     const int nbf = (int)ceil_div(T, kFusedThreads);
     const size_t part_bytes = align_up((size_t)nbf * E_local * sizeof(int32_t), kWsAlign);
     if (E_local <= 64 && ws_bytes >= kWsAlign + part_bytes + (size_t)nbf * sizeof(unsigned long long)) {
-        BatchedFusedArgs fa{topk_idx, T, K, E, E_local, e0, max_num_tokens, tokens_per_expert, slot,
+        BatchedFusedArgs fa{topk_idx, T, K, E, E_local, e0, lim, tokens_per_expert, slot,
                             reinterpret_cast<int32_t *>(wsb + kWsAlign),
                             {reinterpret_cast<unsigned long long *>(wsb + kWsAlign + part_bytes),
                              reinterpret_cast<unsigned long long *>(wsb), next_route_tag()},
@@ -1112,7 +1117,7 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
     batched_count_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E, E_local, e0, part, err);
     if (launch_status() != EP_OK)
         return EP_ERR_CUDA;
-    batched_slot_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E_local, e0, max_num_tokens, part, nb,
+    batched_slot_kernel<<<nb, kRouteThreads, 0, stream>>>(topk_idx, T, K, E_local, e0, lim, part, nb,
                                                           tokens_per_expert, slot, err);
     return launch_status();
 }
@@ -1157,7 +1162,7 @@ extern "C" size_t ep_workspace_size(int64_t T, int K, int P, int E_local, int ch
     const size_t nb = ws_blocks(T, chunks);
     const size_t E = (size_t)P * E_local;
     return kWsAlign + align_up(nb * P * sizeof(int32_t), kWsAlign) + align_up(nb * E * sizeof(int32_t), kWsAlign) +
-           align_up(nb * sizeof(unsigned long long), kWsAlign);
+           align_up(nb * sizeof(unsigned long long), kWsAlign) + align_up(E * sizeof(int32_t), kWsAlign);
 }
 
 extern "C" int ep_chunk_bounds(int64_t T, int chunks, int64_t *h_bounds)

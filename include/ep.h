@@ -11,6 +11,7 @@
  *   [AX] axolotl docs, integrations.expert_parallel.torch_dispatch
  *   [UB] NeMo AutoModel docs, nemo_automodel.components.moe.uccl_ep.buffer
  *   [VB] vLLM docs, vllm.model_executor.layers.fused_moe.prepare_finalize
+ *   [ND] NeMo AutoModel docs, nemo_automodel.components.moe.megatron.token_dispatcher
  *
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless their name starts with h_ (host).
@@ -170,7 +171,7 @@ int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P
                 int64_t num_send, void *recv_x, float *recv_scale, int fp8,
                 int32_t *err, ep_stream_t stream);
 
-/* [AX] combine, [UB] Buffer.combine ("addition without weights"): the local
+/* [AX] combine, [UB] Buffer.combine (an unweighted sum): the local
  * expert kernel has already weighted and summed over K, so
  *   out[t] = sum over p ascending with token_pos[t,p] >= 0 of y[token_pos[t,p]]
  * accumulated in fp32 from +0.0f and rounded once; tokens sent nowhere give
@@ -243,8 +244,45 @@ int ep_batched_prepare_fp8(const void *x, const int64_t *topk_idx, int64_t T, in
                            int32_t *tokens_per_expert, int32_t *slot, int zero_pad,
                            void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
 
+/* The expert-batched prepare with a per-expert capacity and a receive
+ * alignment ([ND] TokenDispatcherConfig: moe_expert_capacity_factor, where
+ * leaving it unset drops nothing, and moe_router_expert_pad_multiple; [UB]
+ * Buffer.dispatch expert_alignment, which makes each local expert's received
+ * count a multiple of it).  ep_batched_prepare and ep_batched_prepare_fp8 are
+ * this call with capacity = 0, alignment = 1, dropped = NULL.
+ *   capacity: 0 = max_num_tokens, with tokens past it dropped and reported as
+ *     EP_ERR_CAPACITY (as ep_batched_prepare); 1 .. max_num_tokens = each local
+ *     expert keeps the first `capacity` tokens naming it, in token order, and
+ *     drops the later ones (slot -1, row not written) without an error: that
+ *     is the capacity's purpose.  ep_expert_capacity gives it from a factor.
+ *   alignment >= 1: tokens_per_expert[e] = min(round_up(kept_e, alignment),
+ *     max_num_tokens) where kept_e is the number of tokens the expert kept;
+ *     rows kept_e .. tokens_per_expert[e]-1 are zero rows (codes 0 and zero
+ *     scale entries for fp8), so a grouped GEMM over the aligned counts reads
+ *     zeros there.  Choose max_num_tokens a multiple of alignment.
+ *   scale_fmt: -1 = bf16 rows (b_rows [E_local, M, H] bf16, b_scale NULL), or
+ *     an EP_SCALE_* layout with round_scale as ep_batched_prepare_fp8 (b_rows
+ *     holds e4m3 codes [E_local, M, H]).
+ *   dropped: [E_local] int32 tokens dropped per expert, or NULL.
+ *   zero_pad: also zero rows (and scale entries) past tokens_per_expert.
+ *   ws: ep_workspace_size(T, K, E / E_local, E_local, 1) bytes.
+ * Host errors: EP_ERR_INVALID_ARG (capacity outside 0..max_num_tokens,
+ * alignment < 1, unknown scale_fmt), EP_ERR_UNSUPPORTED as for
+ * ep_batched_prepare_fp8.  Device errors: EP_ERR_INVALID_EXPERT,
+ * EP_ERR_CAPACITY (capacity = 0 only), EP_ERR_TIMEOUT. */
+int ep_batched_prepare_ex(const void *x, const int64_t *topk_idx, int64_t T, int K, int H,
+                          int E, int E_local, int rank, int max_num_tokens, int capacity, int alignment,
+                          void *b_rows, void *b_scale, int scale_fmt, int round_scale,
+                          int32_t *tokens_per_expert, int32_t *slot, int32_t *dropped, int zero_pad,
+                          void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
+/* Per-expert capacity from a capacity factor (host only): ceil(factor * T * K
+ * / E), the expected tokens per expert scaled by the factor ([ND]
+ * moe_expert_capacity_factor).  -1 for T < 0, K < 1, E < 1 or factor <= 0. */
+int64_t ep_expert_capacity(int64_t T, int K, int E, double factor);
+
 /* [VB] BatchedPrepareAndFinalize.finalize, [UB] Buffer.low_latency_combine
- * ("reduce with weights"): this rank's partial
+ * (a weighted reduction): this rank's partial
  *   out[t] = sum over k ascending with a local expert e_l = topk_idx[t,k] -
  *            rank*E_local and slot[t,k] >= 0 of topk_weights[t,k] * y[e_l, slot[t,k]]
  * with fp32 fused multiply-add from +0.0f, rounded once to bf16; tokens with

@@ -352,7 +352,7 @@ void orc_local_expert_fp8(const uint8_t *q, const float *scale, const int64_t *s
 }
 
 /* ------------------------------------------------------------------------ */
-/* [AX] combine / [UB] Buffer.combine (addition without weights):            */
+/* [AX] combine / [UB] Buffer.combine (an unweighted sum):                  */
 /* out[t] = sum over ranks p ascending with token_pos[t,p] >= 0 of           */
 /*          Y[token_pos[t,p]], accumulated in fp32 from +0.0f, then rounded  */
 /* once to bf16 (out_f32 == 0) or stored as fp32 (out_f32 == 1).  A token    */
@@ -431,7 +431,7 @@ int orc_batched_prepare(const uint16_t *x, const int64_t *topk_idx, int64_t T, i
 }
 
 /* ------------------------------------------------------------------------ */
-/* [VB] finalize / [UB] Buffer.low_latency_combine (reduce with weights):    */
+/* [VB] finalize / [UB] Buffer.low_latency_combine (a weighted reduction):   */
 /* out[t] = sum over k ascending with a local expert e_l = idx[t,k] -        */
 /*          rank*E_local and slot[t,k] >= 0 of w[t,k] * Y[e_l, slot[t,k]],   */
 /* accumulated with fp32 fused multiply-add from +0.0f, rounded once to      */
@@ -464,7 +464,7 @@ void orc_batched_combine(const uint16_t *y, const int64_t *topk_idx, const float
 
 /* ------------------------------------------------------------------------ */
 /* Power-of-two group scales ([UB] Buffer.low_latency_dispatch, round_scale:  */
-/* "round the scaling factors into power of 2"; use_ue8m0: the scale as an    */
+/* the scales rounded to powers of two; use_ue8m0: the scale stored as an    */
 /* UE8M0 code).  Per row and 128-element group g:                            */
 /*   a      = max(max_i |x_i|, 1e-4f)                                        */
 /*   s0     = a / 448.0f                    (fp32, nearest-even)             */
@@ -594,10 +594,10 @@ int orc_batched_prepare_fp8(const uint16_t *x, const int64_t *topk_idx, int64_t 
 
 /* ------------------------------------------------------------------------ */
 /* [VB] prepare (both branches) with a per-expert capacity and a receive      */
-/* alignment ([ND] TokenDispatcherConfig moe_expert_capacity_factor: "the     */
-/* capacity factor for each expert, None means no token will be dropped";     */
-/* [UB] Buffer.dispatch expert_alignment: "align the number of tokens         */
-/* received by each local expert"; [ND] moe_router_expert_pad_multiple).      */
+/* alignment ([ND] TokenDispatcherConfig moe_expert_capacity_factor: a        */
+/* per-expert capacity factor, unset meaning that nothing is dropped;         */
+/* [UB] Buffer.dispatch expert_alignment: the count each local expert         */
+/* receives is made a multiple of it; [ND] moe_router_expert_pad_multiple).   */
 /* Local expert e_l keeps the first `capacity` tokens naming it, in token     */
 /* order (slots 0 .. capacity-1); later ones are dropped (slot -1, row not    */
 /* written) and counted in dropped[e_l]; this is the capacity's purpose, so   */
