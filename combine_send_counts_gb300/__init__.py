@@ -79,6 +79,8 @@ _SIGNATURES = {
     "ep_batched_prepare_ex": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP,
                                      _I32, _I32, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
     "ep_expert_capacity": (_I64, [_I64, _I32, _I32, ctypes.c_double]),
+    "ep_route_nosync_aligned": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I64, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                       _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
 }
 
 EP_SCALE_ROW_F32, EP_SCALE_COL_F32, EP_SCALE_COL_UE8M0 = 0, 1, 2
@@ -207,6 +209,17 @@ def ep_route_nosync(topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, de
                                 _p(tokens_per_expert), _p(send_token_idx), _p(send_rank), _p(send_idx), _p(send_w),
                                 _p(token_pos), _p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream))
     _check(rc, "ep_route_nosync")
+
+
+def ep_route_nosync_aligned(topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, alignment, dest, is_in_rank,
+                            send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx,
+                            send_w, token_pos, ws, err, stream=None):
+    rc = load().ep_route_nosync_aligned(_p(topk_idx), _p(topk_weights), int(T), int(K), int(P), int(E_local),
+                                        int(num_worst_rows), int(alignment), _p(dest), _p(is_in_rank),
+                                        _p(send_counts), _p(rank_offsets), _p(tokens_per_expert),
+                                        _p(send_token_idx), _p(send_rank), _p(send_idx), _p(send_w), _p(token_pos),
+                                        _p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream))
+    _check(rc, "ep_route_nosync_aligned")
 
 
 def ep_dispatch(x, T, H, token_pos, P, num_send, recv_x, recv_scale, fp8, err, stream=None):
@@ -374,12 +387,14 @@ def build_send_layout(topk_idx, topk_weights, dest, is_in_rank, num_send: int, n
 
 
 def route_nosync(topk_idx, topk_weights, num_ranks: int, num_local_experts: int, num_worst_rows: Optional[int] = None,
-                 ws=None, err=None, stream=None, with_tokens_per_expert: bool = True):
+                 ws=None, err=None, stream=None, with_tokens_per_expert: bool = True, alignment: int = 1):
     """Counts and send layout in one call with rows sized for the worst case
-    (no host round trip).  rank_offsets[P] holds the number of rows used."""
+    (no host round trip).  rank_offsets[P] holds the number of rows used.
+    alignment > 1 starts every rank segment at a multiple of it (pad rows
+    carry no token) and rounds tokens_per_expert up."""
     T, K = topk_idx.shape
     P, El = num_ranks, num_local_experts
-    W = T * min(K, P) if num_worst_rows is None else int(num_worst_rows)
+    W = T * min(K, P) + P * (alignment - 1) if num_worst_rows is None else int(num_worst_rows)
     dev = topk_idx.device
     out = dict(
         dest=torch.empty((T, K), dtype=torch.int32, device=dev),
@@ -396,9 +411,9 @@ def route_nosync(topk_idx, topk_weights, num_ranks: int, num_local_experts: int,
     )
     ws = ws if ws is not None else workspace(T, K, P, El, 1, dev)
     err = err if err is not None else error_word(dev)
-    ep_route_nosync(topk_idx, topk_weights, T, K, P, El, W, out["dest"], out["is_in_rank"], out["send_counts"],
-                    out["rank_offsets"], out["tokens_per_expert"], out["send_token_idx"], out["send_rank"],
-                    out["send_idx"], out["send_w"], out["token_pos"], ws, err, stream)
+    ep_route_nosync_aligned(topk_idx, topk_weights, T, K, P, El, W, alignment, out["dest"], out["is_in_rank"],
+                            out["send_counts"], out["rank_offsets"], out["tokens_per_expert"], out["send_token_idx"],
+                            out["send_rank"], out["send_idx"], out["send_w"], out["token_pos"], ws, err, stream)
     out["err"] = err
     return out
 

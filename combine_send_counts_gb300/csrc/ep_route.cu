@@ -257,6 +257,28 @@ __device__ __forceinline__ int nth_set_bit(unsigned m, int r)
 // over blocks bb < b.  Thread i sums rank i % P over every (blockDim/P)-th
 // block, eight loads in flight at a time, then adds into shared memory.
 // The caller zeroes s_tot / s_before and synchronises before and after.
+__device__ __forceinline__ int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Pad rows of an aligned send layout (whole block): rank p's segment holds its
+// rows from rank_start, then pad rows from pad_first[p] up to the next
+// multiple of `align`; a pad row carries no token (token -1, rank p, no
+// experts, zero weights).  Rows at or past num_rows are not written.
+__device__ __forceinline__ void fill_pad_rows(const int32_t *pad_first, int P, int K, int align, int64_t num_rows,
+                              int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w)
+{
+    for (int p = 0; p < P; ++p) {
+        const int64_t lo = pad_first[p], hi = round_up(pad_first[p], align);
+        for (int64_t n = lo + threadIdx.x; n < hi && n < num_rows; n += blockDim.x) {
+            send_token_idx[n] = -1;
+            send_rank[n] = p;
+            for (int k = 0; k < K; ++k) {
+                send_idx[n * K + k] = -1;
+                send_w[n * K + k] = 0.0f;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void block_rank_sums(const int32_t *__restrict__ part, int nb, int P, int b,
                                                 int32_t *s_tot, int32_t *s_before)
 {
@@ -305,6 +327,7 @@ struct LayoutArgs {
     float *send_w;
     int32_t *token_pos;
     int32_t *err;
+    int align;                // rank segments start at multiples of it; tokens_per_expert rounded up
 };
 
 // One block of 256 tokens: the block's first row per rank from the partials,
@@ -330,8 +353,14 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
     if (warp == 0) {
         const int v0 = lane < P ? s_tot[lane] : 0;
         const int v1 = lane + 32 < P ? s_tot[lane + 32] : 0;
-        int e0, e1;
-        const int grand = warp_exclusive_scan64(v0, v1, e0, e1);
+        int e0, e1;   // segment starts: exclusive scan of the aligned counts
+        const int grand = warp_exclusive_scan64(round_up(v0, a.align), round_up(v1, a.align), e0, e1);
+        if (b == 0) {   // first pad row of each segment
+            if (lane < P)
+                s_tot[lane] = e0 + v0;
+            if (lane + 32 < P)
+                s_tot[lane + 32] = e1 + v1;
+        }
         if (lane < P)
             s_base[lane] = e0 + s_before[lane];
         if (lane + 32 < P)
@@ -376,10 +405,13 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
             }
             __syncthreads();
             for (int j = threadIdx.x; j < m; j += blockDim.x)
-                a.tokens_per_expert[b + (j0 + j) * a.nb] = s_tpe[j];
+                a.tokens_per_expert[b + (j0 + j) * a.nb] = round_up(s_tpe[j], a.align);
             __syncthreads();
         }
     }
+    __syncthreads();
+    if (b == 0 && a.align > 1)
+        fill_pad_rows(s_tot, P, K, a.align, a.num_rows, a.send_token_idx, a.send_rank, a.send_idx, a.send_w);
 
     const int64_t t0 = (int64_t)b * kRouteThreads + warp * 32;   // first token of this warp
     const int64_t t = t0 + lane;
@@ -673,6 +705,7 @@ struct FusedArgs {
     int32_t *part_rank;       // [gridDim][P]
     int32_t *part_expert;     // [gridDim][E] when tokens_per_expert is wanted
     GridBarrier bar;
+    int align;                // rank segments start at multiples of it; tokens_per_expert rounded up
     int32_t *err;
 };
 
@@ -801,8 +834,8 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
     if (warp == 0) {
         const int v0 = lane < P ? s_tot[lane] : 0;
         const int v1 = lane + 32 < P ? s_tot[lane + 32] : 0;
-        int e0, e1;
-        const int grand = warp_exclusive_scan64(v0, v1, e0, e1);
+        int e0, e1;   // segment starts: exclusive scan of the aligned counts
+        const int grand = warp_exclusive_scan64(round_up(v0, a.align), round_up(v1, a.align), e0, e1);
         if (lane < P)
             s_base[lane] = e0 + s_before[lane];
         if (lane + 32 < P)
@@ -811,10 +844,12 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
             if (lane < P) {
                 a.send_counts[lane] = v0;
                 a.rank_offsets[lane] = e0;
+                s_tot[lane] = e0 + v0;          // first pad row of the segment
             }
             if (lane + 32 < P) {
                 a.send_counts[lane + 32] = v1;
                 a.rank_offsets[lane + 32] = e1;
+                s_tot[lane + 32] = e1 + v1;
             }
             if (lane == 0) {
                 a.rank_offsets[P] = grand;
@@ -836,10 +871,12 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
             }
             __syncthreads();
             for (int j = threadIdx.x; j < mine; j += blockDim.x)
-                a.tokens_per_expert[b + j * nb] = s_hist[j];
+                a.tokens_per_expert[b + j * nb] = round_up(s_hist[j], a.align);
         }
     }
     __syncthreads();
+    if (b == 0 && a.align > 1)
+        fill_pad_rows(s_tot, P, K, a.align, a.num_rows, a.send_token_idx, a.send_rank, a.send_idx, a.send_w);
 
     if (valid) {
         int32_t *tp = a.token_pos + t * P;
@@ -1266,19 +1303,21 @@ extern "C" int ep_build_send_layout(const int64_t *topk_idx, const float *topk_w
     if (launch_status() != EP_OK)
         return EP_ERR_CUDA;
     LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_send, 1, part_rank, nb,
-                 nullptr, nullptr, nullptr, nullptr, send_token_idx, send_rank, send_idx, send_w, token_pos, err};
+                 nullptr, nullptr, nullptr, nullptr, send_token_idx, send_rank, send_idx, send_w, token_pos, err, 1};
     layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);
     return launch_status();
 }
 
-extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
-                               int E_local, int64_t num_worst_rows, int32_t *dest, uint8_t *is_in_rank,
-                               int32_t *send_counts, int32_t *rank_offsets, int32_t *tokens_per_expert,
-                               int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w,
-                               int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream_)
+static int route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P, int E_local,
+                        int64_t num_worst_rows, int align, int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts,
+                        int32_t *rank_offsets, int32_t *tokens_per_expert, int32_t *send_token_idx,
+                        int32_t *send_rank, int64_t *send_idx, float *send_w, int32_t *token_pos, void *ws,
+                        size_t ws_bytes, int32_t *err, ep_stream_t stream_)
 {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (!routing_shape_ok(T, K, P, E_local) || num_worst_rows < 0 || num_worst_rows >= ((int64_t)1 << 31))
+        return EP_ERR_INVALID_ARG;
+    if (align < 1 || align > (1 << 20))
         return EP_ERR_INVALID_ARG;
     if (ws == nullptr || !aligned(ws, kWsAlign) || ws_bytes < ep_workspace_size(T, K, P, E_local, 1))
         return EP_ERR_INVALID_ARG;
@@ -1306,7 +1345,7 @@ extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weight
     const size_t smem_f = pe != nullptr ? sizeof(int32_t) * E : 0;
     FusedArgs fa{topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
                  rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos,
-                 wl.part_rank, pe, {wl.flags, wl.epoch, next_route_tag()}, err};
+                 wl.part_rank, pe, {wl.flags, wl.epoch, next_route_tag()}, align, err};
     bool launched = false;
     int rc;
     switch (K) {
@@ -1334,9 +1373,32 @@ extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weight
         return EP_ERR_CUDA;
     LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_worst_rows, 0, wl.part_rank, nb,
                  pe, send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
-                 token_pos, err};
+                 token_pos, err, align};
     layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);
     return launch_status();
+}
+
+extern "C" int ep_route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
+                               int E_local, int64_t num_worst_rows, int32_t *dest, uint8_t *is_in_rank,
+                               int32_t *send_counts, int32_t *rank_offsets, int32_t *tokens_per_expert,
+                               int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w,
+                               int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream)
+{
+    return route_nosync(topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, 1, dest, is_in_rank, send_counts,
+                        rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos, ws,
+                        ws_bytes, err, stream);
+}
+
+extern "C" int ep_route_nosync_aligned(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
+                                       int E_local, int64_t num_worst_rows, int alignment, int32_t *dest,
+                                       uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                                       int32_t *tokens_per_expert, int32_t *send_token_idx, int32_t *send_rank,
+                                       int64_t *send_idx, float *send_w, int32_t *token_pos, void *ws,
+                                       size_t ws_bytes, int32_t *err, ep_stream_t stream)
+{
+    return route_nosync(topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, alignment, dest, is_in_rank,
+                        send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
+                        token_pos, ws, ws_bytes, err, stream);
 }
 
 // ====================================================== no-allocation variant ==

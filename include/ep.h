@@ -156,6 +156,27 @@ int ep_route_nosync(const int64_t *topk_idx, const float *topk_weights, int64_t 
                     int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w,
                     int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
 
+/* ep_route_nosync with the receive alignment of [UB] Buffer.dispatch
+ * (expert_alignment) applied to the send layout: every rank's segment starts
+ * at a multiple of `alignment` rows, i.e. rank_offsets is the exclusive scan
+ * of round_up(send_counts[p], alignment) (send_counts stays the true count).
+ * Rank p's rows keep the order of ep_build_send_layout from rank_offsets[p];
+ * the rows after them up to rank_offsets[p+1] are pad rows carrying no token:
+ * send_token_idx -1, send_rank p, send_idx -1, send_w +0 (so a local kernel
+ * over whole segments adds nothing for them; ep_dispatch does not write their
+ * recv_x rows).  token_pos points at the rows in this padded layout, so
+ * ep_dispatch / ep_combine work unchanged.  tokens_per_expert, if requested,
+ * is rounded up to a multiple of `alignment`.
+ *   num_worst_rows: T * min(K, P) + P * (alignment - 1) always suffices.
+ *   alignment >= 1 (1 is ep_route_nosync).
+ * Errors as ep_route_nosync. */
+int ep_route_nosync_aligned(const int64_t *topk_idx, const float *topk_weights, int64_t T, int K, int P,
+                            int E_local, int64_t num_worst_rows, int alignment,
+                            int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                            int32_t *tokens_per_expert,
+                            int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w,
+                            int32_t *token_pos, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
 /* [AX] dispatch on the collective-free local path, [UB] Buffer.dispatch
  * payloads: recv_x[n] = x[t] for every (t, p) with n = token_pos[t,p] >= 0.
  * Each source row is read once and written to each of its rows.

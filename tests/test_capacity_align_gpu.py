@@ -129,3 +129,49 @@ def test_capacity_host_checks():
             ep.batched_prepare_ex(x, idx, 4, 4, 0, 8, **kw)
     with pytest.raises(ep.EPError):
         ep.expert_capacity(8, 2, 4, 0.0)
+
+
+# ------------------------------------------------ aligned send layout (route) --
+# 1M tokens cannot be resident in one cooperative grid, so that case runs the
+# two-launch fallback (count_kernel + layout_write_kernel).
+@pytest.mark.parametrize("T,K,P,El,A", [(1500, 8, 8, 4, 16), (777, 6, 16, 2, 3), (300, 32, 64, 1, 8),
+                                        (5000, 8, 8, 4, 1), (1000000, 2, 4, 8, 128)])
+def test_route_aligned_matches_oracle(T, K, P, El, A):
+    idx, w = routing_inputs(T, K, P * El, 50 + A, 0.1)
+    H = 64
+    x = randn_bf16(T, H, 51)
+    r = ep.route_nosync(idx.cuda(), w.cuda(), P, El, alignment=A)
+    W = r["num_worst_rows"]
+    recv = ep.dispatch_rows(x.cuda(), r["token_pos"], W, err=r["err"])
+    out = ep.combine_rows(recv, r["token_pos"], err=r["err"])
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0
+    c = oracle.compute_send_counts(idx, P, El)
+    lay = oracle.build_send_layout(idx, w, c["dest"], c["is_in_rank"], El)
+    a = oracle.align_send_layout(lay, c["send_counts"], A)
+    n = a["n"]
+    assert_equal("dest", np_(r["dest"]), c["dest"])
+    assert_equal("is_in_rank", np_(r["is_in_rank"]), c["is_in_rank"])
+    assert_equal("send_counts", np_(r["send_counts"]), c["send_counts"])
+    assert_equal("rank_offsets", np_(r["rank_offsets"]), a["rank_offsets"])
+    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), -(-c["tokens_per_expert"] // A) * A)
+    for k in ("send_token_idx", "send_rank", "send_idx"):
+        assert_equal(k, np_(r[k])[:n], a[k])
+    assert_equal("send_w (bits)", np_(r["send_w"])[:n].view(np.uint32), a["send_w"].view(np.uint32))
+    assert_equal("token_pos", np_(r["token_pos"]), a["token_pos"])
+    real = a["send_token_idx"] >= 0
+    assert_equal("recv_x (real rows)", bits16(recv)[:n][real], oracle.dispatch(x, lay["send_token_idx"]))
+    assert_combine_parity("combine", bits16(out), oracle.combine(oracle.dispatch(x, lay["send_token_idx"]),
+                                                                 lay["token_pos"]))
+
+
+def test_route_aligned_capacity_is_flagged():
+    T, K, P, El, A = 900, 8, 8, 4, 64
+    idx, w = routing_inputs(T, K, P * El, 52, 0.0)
+    c = oracle.compute_send_counts(idx, P, El)
+    need = int(sum(-(-int(v) // A) * A for v in c["send_counts"]))
+    r = ep.route_nosync(idx.cuda(), w.cuda(), P, El, alignment=A, num_worst_rows=need - A)
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) & ep.EP_ERR_CAPACITY
+    assert int(r["rank_offsets"][P].item()) == need
+    assert int(r["token_pos"].max().item()) < need - A
