@@ -73,6 +73,7 @@ def _load():
         "orc_batched_prepare_ex": (i32, [P, P, i64, i32, i32, i32, i32, i32, i32, i32, i32, P, P, i32, i32, P, P,
                                          P, i32]),
         "orc_align_send_layout": (i64, [P, i32, i32, i32, i64, P, P, P, P, P, P, P, P, P]),
+        "orc_indices_to_multihot": (i32, [P, P, i64, i32, i32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +289,17 @@ def align_send_layout(layout: dict, send_counts, A: int) -> dict:
     assert got == n
     return dict(n=n, rank_offsets=ro, send_token_idx=a_ti[:n], send_rank=a_r[:n], send_idx=a_i[:n],
                 send_w=a_w[:n], token_pos=a_tp)
+
+
+def indices_to_multihot(topk_idx, topk_probs, E: int):
+    """-> dict(routing_map [T,E] u8, probs [T,E] f32, err)."""
+    idx = _c(topk_idx, np.int64)
+    pr = _c(topk_probs, np.float32)
+    T, K = idx.shape
+    rm = np.empty((T, E), np.uint8)
+    dp = np.empty((T, E), np.float32)
+    err = _load().orc_indices_to_multihot(_ptr(idx), _ptr(pr), T, K, E, _ptr(rm), _ptr(dp))
+    return dict(routing_map=rm, probs=dp, err=int(err))
 
 
 def dispatch_fp8(x, send_token_idx):

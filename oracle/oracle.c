@@ -754,3 +754,38 @@ int64_t orc_align_send_layout(const int32_t *send_counts, int P, int A, int K, i
         }
     return dst;
 }
+
+/* ------------------------------------------------------------------------ */
+/* [ND] _DeepepManager._indices_to_multihot / _HybridEPManager.               */
+/* _indices_to_multihot: top-k indices [T,K] (-1 = masked) and their          */
+/* probabilities [T,K] to a multihot routing map [T,E] and dense              */
+/* probabilities [T,E]:                                                      */
+/*   routing_map[t,e] = 1 iff some slot k of t names e, else 0;               */
+/*   probs[t,e]       = the sum of probs[t,k] over the slots naming e, in     */
+/*                      fp32 from +0.0f in ascending k (a single slot copies  */
+/*                      its probability; reading for repeated ids: the mass   */
+/*                      routed to e), +0.0f where routing_map is 0.           */
+/* An id outside [-1, E) sets error bit 2 and its slot is ignored.            */
+/* ------------------------------------------------------------------------ */
+int orc_indices_to_multihot(const int64_t *topk_idx, const float *topk_probs, int64_t T, int K, int E,
+                            uint8_t *routing_map, float *probs)
+{
+    int err = 0;
+    for (int64_t i = 0; i < T * (int64_t)E; ++i) {
+        routing_map[i] = 0;
+        probs[i] = 0.0f;
+    }
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[t * K + k];
+            if (e == -1)
+                continue;
+            if (e < -1 || e >= E) {
+                err |= ORC_ERR_INVALID_EXPERT;
+                continue;
+            }
+            routing_map[t * E + e] = 1;
+            probs[t * E + e] = probs[t * E + e] + topk_probs[t * K + k];
+        }
+    return err;
+}
