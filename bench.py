@@ -511,7 +511,42 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
         out[name] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab8,
                      "gbs": round(ab8 / us / 1e3, 1), "frac": round(ab8 / us / 1e3 / peak, 4)}
         del r8
+    # capacity factor 1.0 and receive alignment 128 (bf16 rows): kept rows are
+    # copied, the alignment rows zero-filled
+    C = ep.expert_capacity(w.T, w.K, w.E, 1.0)
+    rx = ep.batched_prepare_ex(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, capacity=C, alignment=128, err=err)
+    kept = int((rx["tokens_per_expert"]).sum().item())
+    abx = w.T * w.H * 2 + kept * w.H * 2
+    us = _event_time_us(torch, flush, lambda: ep.ep_batched_prepare_ex(
+        x, idx, w.T, w.K, w.H, w.E, w.E_local, w.rank, w.max_num_tokens, C, 128, rx["b_rows"], None, -1, 0,
+        rx["tokens_per_expert"], rx["slot"], rx["dropped"], 0, ws, err), iters)
+    out["batched_prepare_capacity_align"] = {
+        "workload": "batched, capacity factor 1.0 (%d per expert), alignment 128" % C, "us": round(us, 2),
+        "algorithmic_bytes": abx, "gbs": round(abx / us / 1e3, 1), "frac": round(abx / us / 1e3 / peak, 4),
+        "dropped": int(rx["dropped"].sum().item())}
+    del rx
     del x, y, o, r
+
+    # metadata views of the large workload's routing: multihot map + dense
+    # probabilities, and the send layout with rank segments aligned to 128
+    w = wl.WORKLOADS["large"]
+    idx, wts = (t.to(dev) for t in wl.routing(w))
+    rm = torch.empty((w.T, w.E), dtype=torch.bool, device=dev)
+    pr = torch.empty((w.T, w.E), dtype=torch.float32, device=dev)
+    abm = w.T * w.K * 12 + w.T * w.E * 5
+    us = _event_time_us(torch, flush, lambda: ep.ep_indices_to_multihot(idx, wts, w.T, w.K, w.E, rm, pr, err), iters)
+    out["indices_to_multihot"] = {"workload": "large (T=16384, K=8, E=256)", "us": round(us, 2),
+                                  "algorithmic_bytes": abm, "gbs": round(abm / us / 1e3, 1),
+                                  "frac": round(abm / us / 1e3 / peak, 4)}
+    for A in (1, 128):
+        ra = ep.route_nosync(idx, wts, w.P, w.E_local, alignment=A, err=err)
+        wsr = ep.workspace(w.T, w.K, w.P, w.E_local, 1, dev)
+        us = _event_time_us(torch, flush, lambda: ep.ep_route_nosync_aligned(
+            idx, wts, w.T, w.K, w.P, w.E_local, ra["num_worst_rows"], A, ra["dest"], ra["is_in_rank"],
+            ra["send_counts"], ra["rank_offsets"], None, ra["send_token_idx"], ra["send_rank"], ra["send_idx"],
+            ra["send_w"], ra["token_pos"], wsr, err), iters)
+        out["route_nosync" + ("_aligned128" if A > 1 else "")] = {"workload": "large", "us": round(us, 2)}
+    del rm, pr, ra
 
     w = wl.WORKLOADS["chunk_fp8"]
     idx, wts = (t.to(dev) for t in wl.routing(w))

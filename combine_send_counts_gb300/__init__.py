@@ -81,6 +81,7 @@ _SIGNATURES = {
     "ep_expert_capacity": (_I64, [_I64, _I32, _I32, ctypes.c_double]),
     "ep_route_nosync_aligned": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I64, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                                        _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "ep_indices_to_multihot": (_I32, [_VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP]),
 }
 
 EP_SCALE_ROW_F32, EP_SCALE_COL_F32, EP_SCALE_COL_UE8M0 = 0, 1, 2
@@ -497,6 +498,23 @@ def ep_batched_prepare_ex(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens
                                       _p(dropped), int(zero_pad), _p(ws), ws.numel() * ws.element_size(), _p(err),
                                       _stream(stream))
     _check(rc, "ep_batched_prepare_ex")
+
+
+def ep_indices_to_multihot(topk_idx, topk_probs, T, K, E, routing_map, probs, err, stream=None):
+    rc = load().ep_indices_to_multihot(_p(topk_idx), _p(topk_probs), int(T), int(K), int(E), _p(routing_map),
+                                       _p(probs), _p(err), _stream(stream))
+    _check(rc, "ep_indices_to_multihot")
+
+
+def indices_to_multihot(topk_idx, topk_probs, num_experts: int, err=None, stream=None):
+    """-> (routing_map [T,E] bool, probs [T,E] fp32): the multihot view of top-k routing."""
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    rm = torch.empty((T, num_experts), dtype=torch.bool, device=dev)
+    pr = torch.empty((T, num_experts), dtype=torch.float32, device=dev)
+    err = err if err is not None else error_word(dev)
+    ep_indices_to_multihot(topk_idx, topk_probs, T, K, num_experts, rm, pr, err, stream)
+    return rm, pr
 
 
 def ep_expert_capacity(T: int, K: int, E: int, factor: float) -> int:

@@ -251,12 +251,11 @@ __global__ void zero_scales_kernel(ScaleSpec sp, const int32_t *__restrict__ fir
     const int e = blockIdx.y;
     const int lo = first[e], hi = full ? sp.M : tokens_per_expert[e];
     const int per_row = sp.fmt == EP_SCALE_COL_UE8M0 ? groups / 4 : groups;
-    const int64_t total = (int64_t)sp.M * per_row;
-    uint32_t *base = static_cast<uint32_t *>(sp.out) + (int64_t)e * total;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t s = sp.fmt == EP_SCALE_ROW_F32 ? i / per_row : i % sp.M;
-        if (s >= lo && s < hi)
-            base[i] = 0u;
+    uint32_t *base = static_cast<uint32_t *>(sp.out) + (int64_t)e * sp.M * per_row;
+    const int64_t n = (int64_t)(hi - lo) * per_row;   // entries (slot s in [lo, hi), column c)
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t s = lo + i % (hi - lo), c = i / (hi - lo);
+        base[sp.fmt == EP_SCALE_ROW_F32 ? s * per_row + c : c * sp.M + s] = 0u;
     }
 }
 
@@ -533,13 +532,17 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
     // zero rows: the alignment rows [kept, aligned) always, the rest with zero_pad
     if ((zero_pad || alignment > 1) && M > 0) {
         const int nvec = sp == nullptr ? H / 8 : H / 16;   // 16-byte vectors per row
-        dim3 grid((unsigned)std::min<int64_t>(ceil_div((int64_t)M * nvec, 256), 1024), E_local);
+        // rows an expert may need zeroed: all of them with zero_pad, else
+        // only the alignment rows (fewer than `alignment`)
+        const int64_t zrows = zero_pad ? M : std::min<int64_t>(alignment - 1, M);
+        dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(zrows * nvec, 256), 1024)), E_local);
         zero_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), kept, tokens_per_expert, zero_pad, M,
                                                    nvec);
         if ((rc = launch_status()) != EP_OK)
             return rc;
         if (sp != nullptr) {
-            dim3 sgrid((unsigned)std::min<int64_t>(ceil_div((int64_t)M * (H / 128), 256), 256), E_local);
+            dim3 sgrid((unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(zrows * (H / 128), 256), 256)),
+                       E_local);
             zero_scales_kernel<<<sgrid, 256, 0, stream>>>(*sp, kept, tokens_per_expert, zero_pad, H / 128);
             return launch_status();
         }

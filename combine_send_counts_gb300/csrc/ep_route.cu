@@ -259,14 +259,16 @@ __device__ __forceinline__ int nth_set_bit(unsigned m, int r)
 // The caller zeroes s_tot / s_before and synchronises before and after.
 __device__ __forceinline__ int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Pad rows of an aligned send layout (whole block): rank p's segment holds its
-// rows from rank_start, then pad rows from pad_first[p] up to the next
-// multiple of `align`; a pad row carries no token (token -1, rank p, no
-// experts, zero weights).  Rows at or past num_rows are not written.
+// Pad rows of an aligned send layout (whole block; block b takes ranks b,
+// b + gridDim, ...): rank p's segment holds its rows, then pad rows from
+// pad_first[p] up to the next multiple of `align`; a pad row carries no token
+// (token -1, rank p, no experts, zero weights).  Rows at or past num_rows are
+// not written.
 __device__ __forceinline__ void fill_pad_rows(const int32_t *pad_first, int P, int K, int align, int64_t num_rows,
-                              int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx, float *send_w)
+                                              int32_t *send_token_idx, int32_t *send_rank, int64_t *send_idx,
+                                              float *send_w)
 {
-    for (int p = 0; p < P; ++p) {
+    for (int p = blockIdx.x; p < P; p += gridDim.x) {   // ranks spread over the blocks
         const int64_t lo = pad_first[p], hi = round_up(pad_first[p], align);
         for (int64_t n = lo + threadIdx.x; n < hi && n < num_rows; n += blockDim.x) {
             send_token_idx[n] = -1;
@@ -355,12 +357,10 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
         const int v1 = lane + 32 < P ? s_tot[lane + 32] : 0;
         int e0, e1;   // segment starts: exclusive scan of the aligned counts
         const int grand = warp_exclusive_scan64(round_up(v0, a.align), round_up(v1, a.align), e0, e1);
-        if (b == 0) {   // first pad row of each segment
-            if (lane < P)
-                s_tot[lane] = e0 + v0;
-            if (lane + 32 < P)
-                s_tot[lane + 32] = e1 + v1;
-        }
+        if (lane < P)   // first pad row of each segment
+            s_tot[lane] = e0 + v0;
+        if (lane + 32 < P)
+            s_tot[lane + 32] = e1 + v1;
         if (lane < P)
             s_base[lane] = e0 + s_before[lane];
         if (lane + 32 < P)
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
         }
     }
     __syncthreads();
-    if (b == 0 && a.align > 1)
+    if (a.align > 1)
         fill_pad_rows(s_tot, P, K, a.align, a.num_rows, a.send_token_idx, a.send_rank, a.send_idx, a.send_w);
 
     const int64_t t0 = (int64_t)b * kRouteThreads + warp * 32;   // first token of this warp
@@ -840,16 +840,18 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
             s_base[lane] = e0 + s_before[lane];
         if (lane + 32 < P)
             s_base[lane + 32] = e1 + s_before[lane + 32];
+        if (lane < P)
+            s_tot[lane] = e0 + v0;              // first pad row of the segment
+        if (lane + 32 < P)
+            s_tot[lane + 32] = e1 + v1;
         if (b == 0) {
             if (lane < P) {
                 a.send_counts[lane] = v0;
                 a.rank_offsets[lane] = e0;
-                s_tot[lane] = e0 + v0;          // first pad row of the segment
             }
             if (lane + 32 < P) {
                 a.send_counts[lane + 32] = v1;
                 a.rank_offsets[lane + 32] = e1;
-                s_tot[lane + 32] = e1 + v1;
             }
             if (lane == 0) {
                 a.rank_offsets[P] = grand;
@@ -875,7 +877,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
         }
     }
     __syncthreads();
-    if (b == 0 && a.align > 1)
+    if (a.align > 1)
         fill_pad_rows(s_tot, P, K, a.align, a.num_rows, a.send_token_idx, a.send_rank, a.send_idx, a.send_w);
 
     if (valid) {

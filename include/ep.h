@@ -451,6 +451,22 @@ int ep_local_expert_fp8_dev_callback(void *user, int chunk, int64_t max_rows, co
                                      const int64_t *send_idx, const float *send_w, void *local_out,
                                      int32_t *err, ep_stream_t stream);
 
+/* [ND] _DeepepManager._indices_to_multihot / _HybridEPManager.
+ * _indices_to_multihot: top-k indices and probabilities to the multihot
+ * routing map and the dense probabilities, a second metadata view of the
+ * same topk_idx:
+ *   routing_map[t,e] = 1 iff some slot k of token t names expert e, else 0;
+ *   probs[t,e] = the sum of topk_probs[t,k] over the slots naming e, in fp32
+ *     from +0.0f in ascending k (a single slot copies its probability),
+ *     +0.0f where routing_map is 0.
+ *   topk_idx [T,K] int64 (-1 masked), topk_probs [T,K] fp32 (may be NULL
+ *   when probs is NULL), routing_map [T,E] uint8 or NULL, probs [T,E] fp32 or
+ *   NULL (not both NULL).  One launch, no workspace, no host sync.
+ * Device errors: EP_ERR_INVALID_EXPERT (an id outside [-1, E); the slot is
+ * ignored). */
+int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk_probs, int64_t T, int K, int E,
+                           uint8_t *routing_map, float *probs, int32_t *err, ep_stream_t stream);
+
 /* Same as ep_compute_send_counts, but the caller passes no workspace: the
  * scratch lives in one fixed device array of EP_NOALLOC_SCRATCH_BYTES that the
  * library holds on every device that loads it, until the process exits.  The
