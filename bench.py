@@ -202,23 +202,31 @@ class SendPath:
         self.recv_x = torch.empty((W, w.H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
 
-    def step_nosync(self, y, stream, ev=None):
-        """ev: 4 events (start, after route, after dispatch, after combine) or None."""
+    def step_nosync(self, y, stream, ev=None, split=False):
+        """The no-sync step.  Default: ep_dispatch_nosync (route, then the
+        dispatch launched as its programmatic dependent) and ep_combine; ev: 3
+        events (start, after route + dispatch, after combine) or None.
+        split: ep_route_nosync and ep_dispatch as separate ordinary launches
+        (per-kernel times); ev: 4 events (start, route, dispatch, combine)."""
         ep, w = self.ep, self.w
         T, K, P, El, H, W = w.T, w.K, w.P, w.E_local, w.H, self.W
-        if ev is not None:
-            ev[0].record(stream)
-        ep.ep_route_nosync(self.idx, self.wts, T, K, P, El, W, self.dest, self.is_in_rank, self.send_counts,
-                           self.rank_offsets, None, self.send_token_idx, self.send_rank, self.send_idx, self.send_w,
-                           self.token_pos, self.ws, self.err, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        ep.ep_dispatch(self.x, T, H, self.token_pos, P, W, self.recv_x, None, 0, self.err, stream)
-        if ev is not None:
-            ev[2].record(stream)
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rec(0)
+        if split:
+            ep.ep_route_nosync(self.idx, self.wts, T, K, P, El, W, self.dest, self.is_in_rank, self.send_counts,
+                               self.rank_offsets, None, self.send_token_idx, self.send_rank, self.send_idx,
+                               self.send_w, self.token_pos, self.ws, self.err, stream)
+            rec(1)
+            ep.ep_dispatch(self.x, T, H, self.token_pos, P, W, self.recv_x, None, 0, self.err, stream)
+            rec(2)
+        else:
+            ep.ep_dispatch_nosync(self.x, self.idx, self.wts, T, K, H, P, El, W, 0, self.dest, self.is_in_rank,
+                                  self.send_counts, self.rank_offsets, None, self.send_token_idx, self.send_rank,
+                                  self.send_idx, self.send_w, self.token_pos, self.recv_x, None, self.ws, self.err,
+                                  stream)
+            rec(1)
         ep.ep_combine(y, T, H, self.token_pos, P, W, self.out, 0, self.cws, self.err, stream)
-        if ev is not None:
-            ev[3].record(stream)
+        rec(3 if split else 2)
 
     def step_sync(self, y, stream, ev=None):
         """ev: 6 events (start, counts, host sync, layout, dispatch, combine) or None."""
@@ -245,7 +253,7 @@ class SendPath:
         rec(5)
 
 
-LAUNCHES_PER_STEP = 4   # route: 2 (counts, layout), dispatch: 1, combine: 1
+LAUNCHES_PER_STEP = 3   # route (one cooperative kernel), dispatch, combine
 
 
 def _timed_steps(torch, steps, flush, step, n_events):
@@ -342,16 +350,20 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
-        evs = _timed_steps(torch, args.steps, flush, lambda e: sp.step_nosync(y, stream, e), 4)
+        evs = _timed_steps(torch, args.steps, flush, lambda e: sp.step_nosync(y, stream, e), 3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     if int(sp.err.item()) != 0:
         raise ep.EPError(int(sp.err.item()), "timed steps")
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    parts = {"route": [e[0].elapsed_time(e[1]) for e in evs],
-             "dispatch": [e[1].elapsed_time(e[2]) for e in evs],
-             "combine": [e[2].elapsed_time(e[3]) for e in evs]}
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    combine_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    # per-kernel times: the same step with route and dispatch as separate
+    # ordinary launches (the timed step overlaps them), outside the timed region
+    evs_b = _timed_steps(torch, args.steps, flush, lambda e: sp.step_nosync(y, stream, e, split=True), 4)
+    parts = {"route": [e[0].elapsed_time(e[1]) for e in evs_b],
+             "dispatch": [e[1].elapsed_time(e[2]) for e in evs_b],
+             "combine": combine_ms}
     total_s = sum(step_ms) / 1e3
     tok_s, max_s = aggregate(total_s, float(w.T * args.steps), world, dist if world > 1 else None)
 
@@ -359,7 +371,8 @@ def run_gpu(args):
     ab = algorithmic_bytes(w.T, w.H, N, w.K, w.P)
     ab["route"] = ab.pop("counts") + ab.pop("layout")
     kern = _kernel_table(ab, parts)
-    dom = max(("dispatch", "combine"), key=lambda k: kern[k]["us"])
+    # the roofline kernel: combine, the largest kernel of the step, timed inside the timed steps
+    dom = "combine"
     step_bytes = sum(ab.values())
     achieved_step = step_bytes / (statistics.mean(step_ms) * 1e-3) / 1e9
 
@@ -410,8 +423,9 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write, outside the timed events); "
                          "working set 1.8 GB > L2",
-                   "path": "ep_route_nosync (counts + layout, worst-case rows, no host round trip) -> "
-                           "ep_dispatch -> ep_combine",
+                   "path": "ep_dispatch_nosync (ep_route_nosync: counts + layout, worst-case rows, no host "
+                           "round trip; then the dispatch, launched as the route's programmatic dependent) -> "
+                           "ep_combine",
                    "seed": w.seed},
         "hbm_gbs": round(achieved_step, 1),
         "hbm_frac_of_peak": round(achieved_step / peak, 4),
@@ -420,6 +434,8 @@ def run_gpu(args):
                      "traffic": committed_traffic(dom),
                      "algorithmic_bytes_per_launch": ab[dom]},
         "kernels": kern,
+        "kernels_note": "combine from the timed steps; route and dispatch from the same number of steps run "
+                        "with the two as separate ordinary launches (the timed step overlaps them)",
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
         "host_sync_path": sync_path,

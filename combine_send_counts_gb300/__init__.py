@@ -82,6 +82,8 @@ _SIGNATURES = {
     "ep_route_nosync_aligned": (_I32, [_VP, _VP, _I64, _I32, _I32, _I32, _I64, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                                        _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "ep_indices_to_multihot": (_I32, [_VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "ep_dispatch_nosync": (_I32, [_VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32, _I64, _I32, _VP, _VP, _VP, _VP, _VP,
+                                  _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
 }
 
 EP_SCALE_ROW_F32, EP_SCALE_COL_F32, EP_SCALE_COL_UE8M0 = 0, 1, 2
@@ -498,6 +500,17 @@ def ep_batched_prepare_ex(x, topk_idx, T, K, H, E, E_local, rank, max_num_tokens
                                       _p(dropped), int(zero_pad), _p(ws), ws.numel() * ws.element_size(), _p(err),
                                       _stream(stream))
     _check(rc, "ep_batched_prepare_ex")
+
+
+def ep_dispatch_nosync(x, topk_idx, topk_weights, T, K, H, P, E_local, num_worst_rows, fp8, dest, is_in_rank,
+                       send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
+                       token_pos, recv_x, recv_scale, ws, err, stream=None):
+    rc = load().ep_dispatch_nosync(_p(x), _p(topk_idx), _p(topk_weights), int(T), int(K), int(H), int(P),
+                                   int(E_local), int(num_worst_rows), int(fp8), _p(dest), _p(is_in_rank),
+                                   _p(send_counts), _p(rank_offsets), _p(tokens_per_expert), _p(send_token_idx),
+                                   _p(send_rank), _p(send_idx), _p(send_w), _p(token_pos), _p(recv_x),
+                                   _p(recv_scale), _p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream))
+    _check(rc, "ep_dispatch_nosync")
 
 
 def ep_indices_to_multihot(topk_idx, topk_probs, T, K, E, routing_map, probs, err, stream=None):

@@ -205,8 +205,10 @@ extern "C" int ep_dispatch_chunked_forward_nosync(const void *x, const int64_t *
                              prod_s);
         if (rc != EP_OK)
             return rc;
-        rc = ep_dispatch(static_cast<const char *>(x) + (size_t)s0 * H * 2, len, H, tp_c, P, W, r.recv_x,
-                         fp8 ? r.recv_scale : nullptr, fp8, err, prod_s);
+        // the route just enqueued on the producer stream writes nothing the
+        // dispatch reads before its dependency wait
+        rc = dispatch_rows(static_cast<const char *>(x) + (size_t)s0 * H * 2, len, H, tp_c, P, W, r.recv_x,
+                           fp8 ? r.recv_scale : nullptr, fp8, err, prod, true);
         if (rc != EP_OK)
             return rc;
         if (two && (rc = order_after(ev.ready, prod, cons)) != EP_OK)
@@ -226,4 +228,31 @@ extern "C" int ep_dispatch_chunked_forward_nosync(const void *x, const int64_t *
         }
     }
     return EP_OK;
+}
+
+// ----------------------------------------------- route + dispatch, no sync --
+// ep_route_nosync followed by ep_dispatch into the worst-case rows, with the
+// dispatch launched as a programmatic dependent of the routing kernel: its
+// blocks start loading their input rows while the routing kernel finishes.
+extern "C" int ep_dispatch_nosync(const void *x, const int64_t *topk_idx, const float *topk_weights, int64_t T,
+                                  int K, int H, int P, int E_local, int64_t num_worst_rows, int fp8, int32_t *dest,
+                                  uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                                  int32_t *tokens_per_expert, int32_t *send_token_idx, int32_t *send_rank,
+                                  int64_t *send_idx, float *send_w, int32_t *token_pos, void *recv_x,
+                                  float *recv_scale, void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream)
+{
+    if (fp8 != 0 && fp8 != 1)
+        return EP_ERR_UNSUPPORTED;
+    if (fp8 && H % 128 != 0)
+        return EP_ERR_UNSUPPORTED;
+    if (H < 8 || H % 8 != 0 || (T > 0 && (x == nullptr || !ep::aligned(x, 16))) ||
+        (num_worst_rows > 0 && (recv_x == nullptr || (fp8 && recv_scale == nullptr))))
+        return EP_ERR_INVALID_ARG;
+    int rc = ep_route_nosync(topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
+                             rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos,
+                             ws, ws_bytes, err, stream);
+    if (rc != EP_OK)
+        return rc;
+    return ep::dispatch_rows(x, T, H, token_pos, P, num_worst_rows, recv_x, fp8 ? recv_scale : nullptr, fp8, err,
+                             reinterpret_cast<cudaStream_t>(stream), true);
 }

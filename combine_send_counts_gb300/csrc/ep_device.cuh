@@ -71,6 +71,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 namespace ep {
 
+// --------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialisation may start while the
+// kernel before it in the stream still runs, once every block of that kernel
+// has executed allow_dependents() (or exited).  Before it reads anything the
+// earlier kernel writes it must call grid_dependency_wait(), which returns
+// when the earlier kernel has completed and its writes are visible.  Both are
+// no-ops for ordinary launches.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------- mbarrier + bulk async copy --
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

@@ -53,6 +53,11 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
                          const SlotLimits &lim, int32_t *tokens_per_expert, int32_t *slot,
                          void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream);
 
+// ep_dispatch (ep_move.cu); dependent = launch the scatter as a programmatic
+// dependent of the kernel the library enqueued just before it.
+int dispatch_rows(const void *x, int64_t T, int H, const int32_t *token_pos, int P, int64_t num_send,
+                  void *recv_x, float *recv_scale, int fp8, int32_t *err, cudaStream_t stream, bool dependent);
+
 // The synthetic fp8 expert over N rows (ep_move.cu); with n_rows non-NULL,
 // rows at or past the device value *n_rows are skipped.
 int launch_local_expert_fp8(const uint8_t *recv_q, const float *recv_scale, const int64_t *send_idx,

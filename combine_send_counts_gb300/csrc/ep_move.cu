@@ -12,6 +12,7 @@
 // in one pass for H up to 8*G*U.  The destination (or source) row list of the
 // block's tokens is resolved once into shared memory.
 #include <algorithm>
+#include <utility>
 #include <climits>
 
 #include <cuda_fp16.h>
@@ -69,22 +70,34 @@ scatter_bf16_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows row
 {
     __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
     const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
-    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
-    __syncthreads();
     const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
     const int64_t t = t0 + s;
-    if (s >= g.tpb || t >= T)
+    const bool active = s < g.tpb && t < T;
+    const uint4 *src = x + t * g.nvec;
+    // The rows are inputs, not outputs of the routing kernel before this one:
+    // load the first batch while that kernel may still run (dependent launch).
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int i = lt + u * g.G;
+        if (active && i < g.nvec)
+            v[u] = ld_stream(src + i);
+    }
+    grid_dependency_wait();
+    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
+    __syncthreads();
+    if (!active)
         return;
     const int D = rows.len();
     const int32_t *list = s_rows + s * kMaxList;
-    const uint4 *src = x + t * g.nvec;
     for (int base = 0; base < g.nvec; base += g.G * U) {
-        uint4 v[U];
+        if (base > 0) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + lt + u * g.G;
-            if (i < g.nvec)
-                v[u] = ld_stream(src + i);
+            for (int u = 0; u < U; ++u) {
+                const int i = base + lt + u * g.G;
+                if (i < g.nvec)
+                    v[u] = ld_stream(src + i);
+            }
         }
         for (int j = 0; j < D; ++j) {
             const int32_t r = list[j];
@@ -151,16 +164,21 @@ scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows
 {
     __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
     const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
-    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
-    __syncthreads();
     const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
     const int64_t t = t0 + s;
-    if (s >= g.tpb || t >= T)
+    const bool active = s < g.tpb && t < T;
+    const uint4 *src = x + t * g.nvec;
+    // As a dependent launch the block is resident before the routing kernel
+    // ends; holding the first input vectors across the list loading costs
+    // more registers (occupancy) than it saves here, so wait first.
+    grid_dependency_wait();
+    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
+    __syncthreads();
+    if (!active)
         return;
     const int D = rows.len();
     const int groups = g.nvec / 16;
     const int32_t *list = s_rows + s * kMaxList;
-    const uint4 *src = x + t * g.nvec;
     for (int base = 0; base < g.nvec; base += g.G * U) {
         uint2 q[U];
         float scale[U];
@@ -367,9 +385,29 @@ static Geometry geometry_for(int nvec, int &U)
     return g;
 }
 
+// Launch with programmatic stream serialisation when `dependent` (the kernel
+// may start while the kernel before it runs; used only where the library
+// launched that kernel itself and it writes nothing the early part reads).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_kernel(bool dependent, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <class Rows>
 static int launch_scatter_bf16(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
-                               int err_bits, void *out, int32_t *err, cudaStream_t stream)
+                               int err_bits, void *out, int32_t *err, cudaStream_t stream, bool dependent)
 {
     int U;
     const Geometry g = geometry_for(H / 8, U);
@@ -378,19 +416,25 @@ static int launch_scatter_bf16(const void *x, int64_t T, int H, const Rows &rows
         return EP_OK;
     auto *xs = static_cast<const uint4 *>(x);
     auto *o = static_cast<uint4 *>(out);
+    const dim3 grid((unsigned)blocks), block(g.G * g.tpb);
+    cudaError_t e;
     switch (U) {
-    case 8: scatter_bf16_kernel<8><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
-    case 4: scatter_bf16_kernel<4><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
-    case 2: scatter_bf16_kernel<2><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
-    default: scatter_bf16_kernel<1><<<blocks, g.G * g.tpb, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, o, err); break;
+    case 8: e = launch_kernel(dependent, scatter_bf16_kernel<8, Rows>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, o, err); break;
+    case 4: e = launch_kernel(dependent, scatter_bf16_kernel<4, Rows>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, o, err); break;
+    case 2: e = launch_kernel(dependent, scatter_bf16_kernel<2, Rows>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, o, err); break;
+    default: e = launch_kernel(dependent, scatter_bf16_kernel<1, Rows>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, o, err); break;
     }
-    return launch_status();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
 }
 
 template <class Rows, int SF, bool RS>
 static int launch_scatter_fp8_as(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
                                  int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err,
-                                 cudaStream_t stream)
+                                 cudaStream_t stream, bool dependent)
 {
     int U;
     const Geometry g = geometry_for(H / 8, U);
@@ -399,40 +443,47 @@ static int launch_scatter_fp8_as(const void *x, int64_t T, int H, const Rows &ro
         return EP_OK;
     auto *xs = static_cast<const uint4 *>(x);
     auto *q = static_cast<uint2 *>(out_q);
-    const int nt = g.G * g.tpb;
+    const dim3 grid((unsigned)blocks), block(g.G * g.tpb);
+    cudaError_t e;
     switch (U) {
-    case 8: scatter_fp8_kernel<8, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    case 4: scatter_fp8_kernel<4, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    case 2: scatter_fp8_kernel<2, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    default: scatter_fp8_kernel<1, Rows, SF, RS><<<blocks, nt, 0, stream>>>(xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    case 8: e = launch_kernel(dependent, scatter_fp8_kernel<8, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    case 4: e = launch_kernel(dependent, scatter_fp8_kernel<4, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    case 2: e = launch_kernel(dependent, scatter_fp8_kernel<2, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
+    default: e = launch_kernel(dependent, scatter_fp8_kernel<1, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
     }
-    return launch_status();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
 }
 
 // The send layout only takes row-major plain scales.
 static int launch_scatter_fp8(const void *x, int64_t T, int H, const SendRows &rows, int64_t n_rows,
-                              int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream)
+                              int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream,
+                              bool dependent)
 {
     return launch_scatter_fp8_as<SendRows, EP_SCALE_ROW_F32, false>(x, T, H, rows, n_rows, err_bits, out_q, sp,
-                                                                     err, stream);
+                                                                     err, stream, dependent);
 }
 
 static int launch_scatter_fp8(const void *x, int64_t T, int H, const BatchedRows &rows, int64_t n_rows,
-                              int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream)
+                              int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream,
+                              bool dependent)
 {
     if (sp.fmt == EP_SCALE_COL_UE8M0)
         return launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_UE8M0, true>(x, T, H, rows, n_rows, err_bits,
-                                                                            out_q, sp, err, stream);
+                                                                            out_q, sp, err, stream, dependent);
     if (sp.fmt == EP_SCALE_COL_F32)
         return sp.round ? launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_F32, true>(x, T, H, rows, n_rows, err_bits,
-                                                                                     out_q, sp, err, stream)
+                                                                                     out_q, sp, err, stream, dependent)
                         : launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_F32, false>(x, T, H, rows, n_rows,
                                                                                       err_bits, out_q, sp, err,
-                                                                                      stream);
+                                                                                      stream, dependent);
     return sp.round ? launch_scatter_fp8_as<BatchedRows, EP_SCALE_ROW_F32, true>(x, T, H, rows, n_rows, err_bits,
-                                                                                 out_q, sp, err, stream)
+                                                                                 out_q, sp, err, stream, dependent)
                     : launch_scatter_fp8_as<BatchedRows, EP_SCALE_ROW_F32, false>(x, T, H, rows, n_rows, err_bits,
-                                                                                  out_q, sp, err, stream);
+                                                                                  out_q, sp, err, stream, dependent);
 }
 
 static bool row_shape_ok(int64_t T, int H)
@@ -460,11 +511,12 @@ extern "C" const char *ep_status_str(int status)
     }
 }
 
-extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P,
-                           int64_t num_send, void *recv_x, float *recv_scale, int fp8, int32_t *err,
-                           ep_stream_t stream_)
+namespace ep {
+// ep_dispatch; `dependent` launches the scatter as a programmatic dependent of
+// the routing kernel the library enqueued just before it.
+int dispatch_rows(const void *x, int64_t T, int H, const int32_t *token_pos, int P, int64_t num_send,
+                  void *recv_x, float *recv_scale, int fp8, int32_t *err, cudaStream_t stream, bool dependent)
 {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (!row_shape_ok(T, H) || P < 1 || P > EP_MAX_RANKS || num_send < 0 || num_send >= ((int64_t)1 << 31))
         return EP_ERR_INVALID_ARG;
     if (fp8 != 0 && fp8 != 1)
@@ -482,8 +534,17 @@ extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token
     const SendRows rows{token_pos, P};
     if (fp8)
         return launch_scatter_fp8(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x,
-                                  ScaleSpec{recv_scale, EP_SCALE_ROW_F32, 0, 0}, err, stream);
-    return launch_scatter_bf16(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, err, stream);
+                                  ScaleSpec{recv_scale, EP_SCALE_ROW_F32, 0, 0}, err, stream, dependent);
+    return launch_scatter_bf16(x, T, H, rows, num_send, EP_ERR_COUNT_MISMATCH, recv_x, err, stream, dependent);
+}
+}  // namespace ep
+
+extern "C" int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P,
+                           int64_t num_send, void *recv_x, float *recv_scale, int fp8, int32_t *err,
+                           ep_stream_t stream)
+{
+    return dispatch_rows(x, T, H, token_pos, P, num_send, recv_x, recv_scale, fp8, err,
+                         reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 // bf16 rows (sp == nullptr) or fp8 codes with scales as *sp; capacity 0
@@ -524,8 +585,9 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
     if (T > 0) {
         const BatchedRows rows{topk_idx, slot, nullptr, K, (int64_t)rank * E_local, E_local, M, true};
         const int64_t n_rows = (int64_t)E_local * M;
-        rc = sp == nullptr ? launch_scatter_bf16(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, err, stream)
-                           : launch_scatter_fp8(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, *sp, err, stream);
+        // the slot kernel just enqueued writes nothing the scatter reads early
+        rc = sp == nullptr ? launch_scatter_bf16(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, err, stream, true)
+                           : launch_scatter_fp8(x, T, H, rows, n_rows, EP_ERR_CAPACITY, b_x, *sp, err, stream, true);
         if (rc != EP_OK)
             return rc;
     }

@@ -338,6 +338,7 @@ struct LayoutArgs {
 // rank p are consecutive, so the warp covers them with consecutive stores.
 __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs a)
 {
+    allow_dependents();   // the dispatch after this kernel may start loading its input rows
     __shared__ int32_t s_base[EP_MAX_RANKS];
     __shared__ int32_t s_tot[EP_MAX_RANKS], s_before[EP_MAX_RANKS];
     __shared__ int32_t s_warp[kWarps][EP_MAX_RANKS];
@@ -551,6 +552,7 @@ batched_slot_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E_loc
                     const int32_t *__restrict__ part, int nb, int32_t *__restrict__ tokens_per_expert,
                     int32_t *__restrict__ slot, int32_t *err)
 {
+    allow_dependents();   // the row scatter after this kernel may start loading its input rows
     __shared__ int32_t s_base[kGroup], s_tot[kGroup];
     __shared__ int32_t s_warp[kWarps][kGroup];
     const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
@@ -713,6 +715,7 @@ struct FusedArgs {
 template <int KC>
 __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
 {
+    allow_dependents();   // the dispatch after this kernel may start loading its input rows
     constexpr int KM = KC > 0 ? KC : EP_MAX_TOPK;
     extern __shared__ int32_t s_hist[];          // [E] when counting experts
     __shared__ int32_t s_warp[kFusedWarps][EP_MAX_RANKS];
@@ -992,6 +995,7 @@ struct BatchedFusedArgs {
 template <int KC>
 __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFusedArgs a)
 {
+    allow_dependents();   // the row scatter after this kernel may start loading its input rows
     constexpr int KM = KC > 0 ? KC : EP_MAX_TOPK;
     __shared__ int32_t s_warp[kFusedWarps][64];
     __shared__ int32_t s_tot[64], s_before[64];

@@ -192,6 +192,21 @@ int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P
                 int64_t num_send, void *recv_x, float *recv_scale, int fp8,
                 int32_t *err, ep_stream_t stream);
 
+/* [UB] Buffer.dispatch in num_worst_tokens mode on the collective-free path:
+ * ep_route_nosync (all its outputs, rows sized num_worst_rows) followed by
+ * ep_dispatch of x into recv_x (bf16, or fp8 codes + scales when fp8 = 1),
+ * in one call.  The dispatch is launched as a programmatic dependent of the
+ * routing kernel, so its blocks load their input rows while routing
+ * finishes; x must therefore be complete before the call (it is read by the
+ * dispatch before the routing kernel ends, never written by it).  Arguments
+ * and errors as the two calls; recv_scale is used only with fp8 = 1. */
+int ep_dispatch_nosync(const void *x, const int64_t *topk_idx, const float *topk_weights, int64_t T, int K,
+                       int H, int P, int E_local, int64_t num_worst_rows, int fp8,
+                       int32_t *dest, uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
+                       int32_t *tokens_per_expert, int32_t *send_token_idx, int32_t *send_rank,
+                       int64_t *send_idx, float *send_w, int32_t *token_pos, void *recv_x, float *recv_scale,
+                       void *ws, size_t ws_bytes, int32_t *err, ep_stream_t stream);
+
 /* [AX] combine, [UB] Buffer.combine (an unweighted sum): the local
  * expert kernel has already weighted and summed over K, so
  *   out[t] = sum over p ascending with token_pos[t,p] >= 0 of y[token_pos[t,p]]

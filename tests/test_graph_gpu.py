@@ -31,8 +31,9 @@ def _capture(fn, stream):
     return g
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("T,H,K,P,El", [(5000, 256, 8, 8, 4), (1537, 136, 6, 16, 2)])
-def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El):
+def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El, fused):
     dev = "cuda"
     W = T * min(K, P)
     idx = torch.empty((T, K), dtype=torch.int64, device=dev)
@@ -56,9 +57,13 @@ def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El):
 
     def step():
         s = torch.cuda.current_stream()
-        ep.ep_route_nosync(idx, wts, T, K, P, El, W, o_dest, o_iir, o_sc, o_ro, o_tpe, o_sti, o_sr, o_si, o_sw,
-                           o_tp, ws, err, s)
-        ep.ep_dispatch(x, T, H, o_tp, P, W, recv, None, 0, err, s)
+        if fused:   # route, then the dispatch as its programmatic dependent
+            ep.ep_dispatch_nosync(x, idx, wts, T, K, H, P, El, W, 0, o_dest, o_iir, o_sc, o_ro, o_tpe, o_sti, o_sr,
+                                  o_si, o_sw, o_tp, recv, None, ws, err, s)
+        else:
+            ep.ep_route_nosync(idx, wts, T, K, P, El, W, o_dest, o_iir, o_sc, o_ro, o_tpe, o_sti, o_sr, o_si, o_sw,
+                               o_tp, ws, err, s)
+            ep.ep_dispatch(x, T, H, o_tp, P, W, recv, None, 0, err, s)
         # combine the received rows themselves: out[t] = (ranks of t) * x[t]
         ep.ep_combine(recv, T, H, o_tp, P, W, out, 0, cws, err, s)
 

@@ -666,3 +666,47 @@ def test_batched_prepare_many_local_experts():
     assert int(r["err"].item()) == 0
     assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), o["tokens_per_expert"])
     assert_equal("slot", np_(r["slot"]), o["slot"])
+
+
+# ----------------------------------- route + dispatch as one no-sync call --
+@pytest.mark.parametrize("name,fp8", [("mid", False), ("large", False), ("chunk_fp8", True)])
+def test_dispatch_nosync_matches_oracle(name, fp8):
+    w = wl.WORKLOADS[name]
+    if name == "chunk_fp8":
+        w = w.scaled(T=3000)
+    x, idx, wts = wl.make(w)
+    dev = "cuda"
+    T, K, P, El, H = w.T, w.K, w.P, w.E_local, w.H
+    W = T * min(K, P)
+    i32 = torch.int32
+    outs = dict(dest=torch.empty((T, K), dtype=i32, device=dev),
+                is_in_rank=torch.empty((T, P), dtype=torch.uint8, device=dev),
+                send_counts=torch.empty(P, dtype=i32, device=dev),
+                rank_offsets=torch.empty(P + 1, dtype=i32, device=dev),
+                send_token_idx=torch.empty(W, dtype=i32, device=dev),
+                send_rank=torch.empty(W, dtype=i32, device=dev),
+                send_idx=torch.empty((W, K), dtype=torch.int64, device=dev),
+                send_w=torch.empty((W, K), dtype=torch.float32, device=dev),
+                token_pos=torch.empty((T, P), dtype=i32, device=dev))
+    recv = torch.empty((W, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    scale = torch.empty((W, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+    err = ep.error_word()
+    ep.ep_dispatch_nosync(x.to(dev), idx.to(dev), wts.to(dev), T, K, H, P, El, W, int(fp8), outs["dest"],
+                          outs["is_in_rank"], outs["send_counts"], outs["rank_offsets"], None, outs["send_token_idx"],
+                          outs["send_rank"], outs["send_idx"], outs["send_w"], outs["token_pos"], recv, scale,
+                          ep.workspace(T, K, P, El), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o = oracle.send_path(x, idx, wts, None, P, El)
+    ol = o["layout"]
+    N = ol["n"]
+    assert int(outs["rank_offsets"][P].item()) == N
+    for k in ("send_token_idx", "send_rank", "send_idx"):
+        assert_equal(k, np_(outs[k])[:N], ol[k])
+    assert_equal("token_pos", np_(outs["token_pos"]), ol["token_pos"])
+    if fp8:
+        q, sc = oracle.dispatch_fp8(x, ol["send_token_idx"])
+        assert_equal("fp8 codes", np_(recv)[:N], q)
+        assert_equal("fp8 scales (bits)", np_(scale)[:N].view(np.uint32), sc.view(np.uint32))
+    else:
+        assert_equal("recv_x", bits16(recv)[:N], o["recv_x"])
