@@ -12,7 +12,8 @@ under ``host_sync_path``, and a CUDA-graph replay of the step under
 
 on the large skewed workload (T=16384, H=7168 bf16, E=256, K=8, P=8 logical
 ranks, Zipf(1.2) routing).  Inputs are resident in HBM when a step starts; L2
-is flushed (512 MiB write) between steps, outside the timed events.
+is flushed between steps (512 MiB write, then a 256 MiB read that leaves L2
+clean), outside the timed events.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (plain C, one core) on the same workload instead.
@@ -36,6 +37,23 @@ if ROOT not in sys.path:
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
+L2_CLEAN_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2 (evicts every line
+    the step could reuse), then read another one, so that the lines L2 holds
+    are clean and the next step pays for no write-back of the flush's data."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.rbuf = torch.ones(L2_CLEAN_BYTES, dtype=torch.uint8, device=dev)
+        self.acc = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.wbuf.zero_()
+        self.torch.sum(self.rbuf, dim=0, dtype=self.torch.int64, out=self.acc[0])
 
 
 # ------------------------------------------------------------ host helpers --
@@ -259,7 +277,7 @@ LAUNCHES_PER_STEP = 3   # route (one cooperative kernel), dispatch, combine
 def _timed_steps(torch, steps, flush, step, n_events):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(steps)]
     for k in range(steps):
-        flush.zero_()          # outside the events; the step is enqueued while it runs
+        flush()                # outside the events; the step is enqueued while it runs
         step(evs[k])
     torch.cuda.synchronize()
     return evs
@@ -289,7 +307,7 @@ def _graph_replay(torch, sp, y, stream, flush, dev, steps, T, step_bytes):
     torch.cuda.synchronize()
     gt = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         g.replay()
@@ -334,12 +352,12 @@ def run_gpu(args):
     y_h = wl.expert_outputs(w, N)
     y = torch.empty((sp.W, w.H), dtype=torch.bfloat16, device=dev)   # expert outputs in worst-case rows
     y[:N].copy_(y_h)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
 
     for _ in range(max(args.warmup, 0)):
-        flush.zero_()
+        flush()
         sp.step_nosync(y, stream)
-        flush.zero_()
+        flush()
         sp.step_sync(y, stream)
     torch.cuda.synchronize()
     if int(sp.err.item()) != 0:
@@ -421,8 +439,8 @@ def run_gpu(args):
                                f"routing={w.routing}({w.zipf_s}) weights={w.weights}",
                    "N_rows": N, "worst_case_rows": sp.W,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (512 MiB write, outside the timed events); "
-                         "working set 1.8 GB > L2",
+                   "l2": "flushed between steps, outside the timed events: a 512 MiB write, then a 256 MiB "
+                         "read so that L2 holds no dirty lines; working set 1.8 GB > L2",
                    "path": "ep_dispatch_nosync (ep_route_nosync: counts + layout, worst-case rows, no host "
                            "round trip; then the dispatch, launched as the route's programmatic dependent) -> "
                            "ep_combine",
@@ -460,7 +478,7 @@ def run_gpu(args):
 def _event_time_us(torch, flush, fn, iters, warmup=2):
     ts = []
     for i in range(warmup + iters):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -711,7 +729,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-warmup", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-steps", type=int, default=4)
+    ap.add_argument("--cpu-steps", type=int, default=20, help="oracle steps of the CPU baseline (about 0.5 s each on one core)")
     ap.add_argument("--reference-tokens", type=int, default=4096)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
