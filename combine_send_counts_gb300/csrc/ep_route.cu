@@ -629,12 +629,14 @@ __device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned l
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
 {
     unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Grid barrier of the cooperative routing kernels.  A launch's tag mixes the
 // host's per-call tag with a launch counter kept in the workspace header, so
@@ -662,7 +664,8 @@ __device__ __forceinline__ unsigned long long barrier_tag(const GridBarrier &g, 
 // blocks will read.
 __device__ __forceinline__ void barrier_arrive(const GridBarrier &g, unsigned long long tag)
 {
-    __threadfence();
+    // st.release orders before the flag every write of this thread and, via
+    // the preceding __syncthreads, of the whole block (release is cumulative)
     st_release_u64(&g.flags[blockIdx.x], tag);
 }
 
@@ -671,12 +674,15 @@ __device__ __forceinline__ void barrier_arrive(const GridBarrier &g, unsigned lo
 // before the block's first __syncthreads.
 __device__ __forceinline__ bool barrier_wait(const GridBarrier &g, unsigned long long tag, unsigned long long e, int *s_fail)
 {
+    // spin with relaxed loads; one acquire fence once every flag was seen
+    // (pairs with the release of barrier_arrive), then __syncthreads carries
+    // the ordering to the rest of the block
     bool ok = true;
     for (int i = threadIdx.x; i < (int)gridDim.x && ok; i += blockDim.x) {
-        if (ld_acquire_u64(&g.flags[i]) == tag)
+        if (ld_relaxed_u64(&g.flags[i]) == tag)
             continue;
         const uint64_t t0 = global_timer_ns();
-        while (ld_acquire_u64(&g.flags[i]) != tag)
+        while (ld_relaxed_u64(&g.flags[i]) != tag)
             if (global_timer_ns() - t0 > kBarrierNs) {
                 ok = false;
                 break;
@@ -684,7 +690,7 @@ __device__ __forceinline__ bool barrier_wait(const GridBarrier &g, unsigned long
     }
     if (!ok)
         *s_fail = 1;
-    __threadfence();
+    fence_acq_rel_gpu();
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *reinterpret_cast<volatile unsigned long long *>(g.epoch) = e + 1;
@@ -1031,11 +1037,22 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
         if (el >= 0 && el < El)
             mask |= 1ull << el;
     }
+    // The ballot of expert e is the warp's bit column for e: lane e & 31 keeps
+    // it (word e < 32 in bal_lo, else bal_hi) for the slot phase.
+    unsigned bal_lo = 0, bal_hi = 0;
     for (int e = 0; e < El; ++e) {
         const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
-        if (lane == 0)
-            s_warp[warp][e] = __popc(bal);
+        if (lane == (e & 31)) {
+            if (e < 32)
+                bal_lo = bal;
+            else
+                bal_hi = bal;
+        }
     }
+    if (lane < El)
+        s_warp[warp][lane] = __popc(bal_lo);
+    if (lane + 32 < El)
+        s_warp[warp][lane + 32] = __popc(bal_hi);
     __syncthreads();
     if (threadIdx.x < El) {
         int run = 0;
@@ -1063,22 +1080,29 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
     __syncthreads();
     if (b == 0 && threadIdx.x < El)
         bad |= finish_expert_count(a.lim, threadIdx.x, s_tot[threadIdx.x], a.tokens_per_expert);
+    // slot of this token for expert e: the expert's block base, this warp's
+    // base within the block, and the token's rank among the warp's lanes
+    // naming e (lanes below it in e's ballot word); words and bases are held
+    // by lane e & 31 and fetched by shuffle, so every lane takes the same path
+    const int base_lo = lane < El ? s_before[lane] + s_warp[warp][lane] : 0;
+    const int base_hi = lane + 32 < El ? s_before[lane + 32] + s_warp[warp][lane + 32] : 0;
     int32_t sl[KM];
 #pragma unroll
-    for (int k = 0; k < KM; ++k)
+    for (int k = 0; k < KM; ++k) {
         sl[k] = -1;
-    for (int e = 0; e < El; ++e) {
-        const unsigned bal = __ballot_sync(kFull, (mask >> e) & 1ull);
-        if (!((mask >> e) & 1ull))
+        if (k >= K)
             continue;
-        const int s = s_before[e] + s_warp[warp][e] + __popc(bal & lanemask_lt());
-        const int v = s < a.lim.cap ? s : -1;
+        const int64_t el = id[k] - a.e0;
+        const bool local = el >= 0 && el < El;
+        const int src = local ? (int)(el & 31) : 0;
+        const unsigned w_lo = __shfl_sync(kFull, bal_lo, src), w_hi = __shfl_sync(kFull, bal_hi, src);
+        const int b_lo = __shfl_sync(kFull, base_lo, src), b_hi = __shfl_sync(kFull, base_hi, src);
+        if (!valid || !local)
+            continue;
+        const int s = (el < 32 ? b_lo : b_hi) + __popc((el < 32 ? w_lo : w_hi) & lanemask_lt());
+        sl[k] = s < a.lim.cap ? s : -1;
         if (s >= a.lim.cap && !a.lim.silent)
             bad = EP_ERR_CAPACITY;
-#pragma unroll
-        for (int k = 0; k < KM; ++k)
-            if (k < K && id[k] == a.e0 + e)
-                sl[k] = v;
     }
     if (valid) {
 #pragma unroll
