@@ -48,12 +48,12 @@ class L2Flush:
     def __init__(self, torch, dev):
         self.torch = torch
         self.wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        self.rbuf = torch.ones(L2_CLEAN_BYTES, dtype=torch.uint8, device=dev)
-        self.acc = torch.empty(1, dtype=torch.int64, device=dev)
+        self.rbuf = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)   # summed as is: one read
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
 
     def __call__(self):
         self.wbuf.zero_()
-        self.torch.sum(self.rbuf, dim=0, dtype=self.torch.int64, out=self.acc[0])
+        self.torch.sum(self.rbuf, dim=0, out=self.acc)
 
 
 # ------------------------------------------------------------ host helpers --
