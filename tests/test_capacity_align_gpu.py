@@ -175,3 +175,18 @@ def test_route_aligned_capacity_is_flagged():
     assert int(r["err"].item()) & ep.EP_ERR_CAPACITY
     assert int(r["rank_offsets"][P].item()) == need
     assert int(r["token_pos"].max().item()) < need - A
+
+
+@pytest.mark.parametrize("fmt,rs,C,A", [(None, False, 0, 1), (1, False, 0, 1), (2, True, 30, 8), (None, False, 25, 4)])
+def test_repeated_expert_ids_write_one_row(fmt, rs, C, A):
+    # tokens naming one local expert in several slots: one row per (expert,
+    # token), every such slot gets the same slot value; several tokens per
+    # block (short rows), so the row-list dedup spans a block's tokens
+    T, H, K, E, El, rank, M = 700, 512, 6, 12, 4, 1, 300
+    idx, _ = routing_inputs(T, K, E, 61, 0.1, dup=True)
+    x = randn_bf16(T, H, 62)
+    o, g = _run(x, idx, E, El, rank, M, C, A, fmt, rs, True)
+    assert o["err"] == 0
+    overflow = C == 0 and int(o["dropped"].sum()) > 0
+    assert int(g["err"].item()) == (ep.EP_ERR_CAPACITY if overflow else 0)
+    _compare(o, g, fmt is not None)
