@@ -156,93 +156,111 @@ __device__ __forceinline__ void put_scale(const ScaleSpec &sp, int64_t base, int
 //   power of two: scale = 2^e, the smallest power of two >= a / 448 (from the
 //                 bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
 //                 UE8M0 code e + 127.
-// SF: the scale layout (EP_SCALE_*); RS: power-of-two scales.
+// fp8 (1x128) scatter, one warp per token (grid-stride loop over tokens).
+// Lanes j < D (and j + 32) resolve the token's rows; the warp quantises the
+// row once, in chunks of U 16-byte vectors per lane, where lanes 0-15 and
+// 16-31 each hold one 128-element group (group max by half-warp shuffles), and
+// writes each chunk's e4m3 codes and group scales to every row, taking the
+// rows by shuffle.  No shared memory and no block barrier.  With
+// a = max(max|x|, 1e-4):
+//   plain (RS = false): q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448;
+//   power of two:       scale = 2^e, the smallest power of two >= a / 448 (from
+//                       the bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
+//                       UE8M0 code e + 127.
+// SF is the scale layout (EP_SCALE_*).
 template <int U, class Rows, int SF, bool RS>
 __global__ void __launch_bounds__(kMoveThreads)
-scatter_fp8_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows rows, int64_t n_rows,
-                   int err_bits, uint2 *__restrict__ out_q, ScaleSpec sp, int32_t *err)
+scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows rows, int64_t n_rows,
+                        int err_bits, uint2 *__restrict__ out_q, ScaleSpec sp, int32_t *err)
 {
-    __shared__ int32_t s_rows[kMaxTokensPerBlock * kMaxList];
-    const int64_t t0 = (int64_t)blockIdx.x * g.tpb;
-    const int s = threadIdx.x / g.G, lt = threadIdx.x % g.G;
-    const int64_t t = t0 + s;
-    const bool active = s < g.tpb && t < T;
-    const uint4 *src = x + t * g.nvec;
-    // As a dependent launch the block is resident before the routing kernel
-    // ends; holding the first input vectors across the list loading costs
-    // more registers (occupancy) than it saves here, so wait first.
     grid_dependency_wait();
-    load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
-    __syncthreads();
-    if (!active)
-        return;
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int D = rows.len();
-    const int groups = g.nvec / 16;
-    const int32_t *list = s_rows + s * kMaxList;
-    for (int base = 0; base < g.nvec; base += g.G * U) {
-        uint2 q[U];
-        float scale[U];
-        uint32_t code[U];
-        uint4 vin[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {            // all loads first: U vectors in flight
-            const int i = base + lt + u * g.G;
-            vin[u] = make_uint4(0, 0, 0, 0);
-            if (i < g.nvec)
-                vin[u] = ld_stream(src + i);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint4 v = vin[u];                // invalid vectors are whole half-warps of zeros
-            float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                          bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-            float amax = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                amax = fmaxf(amax, fabsf(f[e]));
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-            const float a = fmaxf(amax, 1e-4f);
-            float inv;
-            if (RS) {
-                // a / 448 is a positive normal fp32: round its exponent up
-                // unless the mantissa is zero
-                const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
-                const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
-                scale[u] = __uint_as_float(eb << 23);
-                inv = __uint_as_float((254u - eb) << 23);
-                code[u] = eb;
-            } else {
-                inv = __fdiv_rn(448.0f, a);
-                scale[u] = __fdiv_rn(a, 448.0f);
-                code[u] = 0;
+    const int groups = nvec / 16;
+    int bad = 0;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
+        int32_t r_lo = -1, r_hi = -1;
+        if (lane < D) {
+            r_lo = rows.row(t, lane);
+            if (r_lo >= n_rows) {
+                bad = err_bits;
+                r_lo = -1;
             }
-            uint32_t packed[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 pr = make_float2(__fmul_rn(f[2 * e], inv), __fmul_rn(f[2 * e + 1], inv));
-                packed[e] = (uint32_t)__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
-            }
-            q[u] = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
         }
-        for (int j = 0; j < D; ++j) {
-            const int32_t r = list[j];
-            if (r < 0)
-                continue;
-            uint2 *dq = out_q + (int64_t)r * g.nvec;
-            const int64_t sb = scale_row_base<SF>(sp, r, groups);
+        if (lane + 32 < D) {
+            r_hi = rows.row(t, lane + 32);
+            if (r_hi >= n_rows) {
+                bad = err_bits;
+                r_hi = -1;
+            }
+        }
+        const uint64_t valid =
+            (uint64_t)__ballot_sync(kFull, r_lo >= 0) | ((uint64_t)__ballot_sync(kFull, r_hi >= 0) << 32);
+        const uint4 *src = x + t * nvec;
+        for (int base = 0; base < nvec; base += 32 * U) {
+            uint4 vin[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {   // all loads first: U vectors in flight
+                const int i = base + lane + 32 * u;
+                vin[u] = make_uint4(0, 0, 0, 0);
+                if (i < nvec)
+                    vin[u] = ld_stream(src + i);
+            }
+            uint2 q[U];
+            float scale[U];
+            uint32_t code[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int i = base + lt + u * g.G;
-                if (i < g.nvec) {
-                    st_stream(dq + i, q[u]);
-                    if ((lt & 15) == 0)
-                        put_scale<SF>(sp, sb, i >> 4, scale[u], code[u]);
+                const uint4 v = vin[u];            // vectors past the row are whole half-warps of zeros
+                float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+                float amax = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+                const float a = fmaxf(amax, 1e-4f);
+                float inv;
+                if (RS) {
+                    const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
+                    const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
+                    scale[u] = __uint_as_float(eb << 23);
+                    inv = __uint_as_float((254u - eb) << 23);
+                    code[u] = eb;
+                } else {
+                    inv = __fdiv_rn(448.0f, a);
+                    scale[u] = __fdiv_rn(a, 448.0f);
+                    code[u] = 0;
+                }
+                uint32_t packed[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 pr = make_float2(__fmul_rn(f[2 * e], inv), __fmul_rn(f[2 * e + 1], inv));
+                    packed[e] = (uint32_t)__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
+                }
+                q[u] = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
+            }
+            for (uint64_t m = valid; m != 0; m &= m - 1) {   // warp-uniform
+                const int j = __ffsll((long long)m) - 1;
+                const int32_t r = j < 32 ? __shfl_sync(kFull, r_lo, j) : __shfl_sync(kFull, r_hi, j - 32);
+                uint2 *dq = out_q + (int64_t)r * nvec;
+                const int64_t sb = scale_row_base<SF>(sp, r, groups);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = base + lane + 32 * u;
+                    if (i < nvec) {
+                        st_stream(dq + i, q[u]);
+                        if ((lane & 15) == 0)
+                            put_scale<SF>(sp, sb, i >> 4, scale[u], code[u]);
+                    }
                 }
             }
         }
     }
+    raise(err, bad);
 }
 
 // ------------------------------------------------------------- zero padding --
@@ -405,6 +423,19 @@ static cudaError_t launch_kernel(bool dependent, void (*kernel)(KArgs...), dim3 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+static int device_sms()
+{
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sms = 152;
+        }
+    }
+    return sms;
+}
+
 template <class Rows>
 static int launch_scatter_bf16(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
                                int err_bits, void *out, int32_t *err, cudaStream_t stream, bool dependent)
@@ -431,26 +462,25 @@ static int launch_scatter_bf16(const void *x, int64_t T, int H, const Rows &rows
     return EP_OK;
 }
 
+
 template <class Rows, int SF, bool RS>
 static int launch_scatter_fp8_as(const void *x, int64_t T, int H, const Rows &rows, int64_t n_rows,
                                  int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err,
                                  cudaStream_t stream, bool dependent)
 {
-    int U;
-    const Geometry g = geometry_for(H / 8, U);
-    const int64_t blocks = ceil_div(T, g.tpb);
+    const int nvec = H / 8;
+    const int64_t warps = kMoveThreads / 32;
+    const int64_t blocks = std::min<int64_t>(ceil_div(T, warps), (int64_t)8 * device_sms());
     if (blocks == 0)
         return EP_OK;
     auto *xs = static_cast<const uint4 *>(x);
     auto *q = static_cast<uint2 *>(out_q);
-    const dim3 grid((unsigned)blocks), block(g.G * g.tpb);
-    cudaError_t e;
-    switch (U) {
-    case 8: e = launch_kernel(dependent, scatter_fp8_kernel<8, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    case 4: e = launch_kernel(dependent, scatter_fp8_kernel<4, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    case 2: e = launch_kernel(dependent, scatter_fp8_kernel<2, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    default: e = launch_kernel(dependent, scatter_fp8_kernel<1, Rows, SF, RS>, grid, block, 0, stream, xs, T, g, rows, n_rows, err_bits, q, sp, err); break;
-    }
+    const dim3 grid((unsigned)blocks), block(kMoveThreads);
+    const cudaError_t e =
+        nvec > 64 ? launch_kernel(dependent, scatter_fp8_warp_kernel<4, Rows, SF, RS>, grid, block, 0, stream, xs, T,
+                                  nvec, rows, n_rows, err_bits, q, sp, err)
+                  : launch_kernel(dependent, scatter_fp8_warp_kernel<2, Rows, SF, RS>, grid, block, 0, stream, xs, T,
+                                  nvec, rows, n_rows, err_bits, q, sp, err);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return EP_ERR_CUDA;
