@@ -195,6 +195,7 @@ EDGE = [
     (777, 512, 1, 16, 4, 0.25, False),       # K = 1: counting sort
     (513, 1024, 6, 8, 8, 1.0, False),        # nothing routed
     (300, 16384, 4, 4, 4, 0.0, False),       # a row longer than one pass of the block
+    (1000, 64, 8, 64, 128, 0.1, False),      # E = P * E_local = 8192, the largest expert count
 ]
 
 
