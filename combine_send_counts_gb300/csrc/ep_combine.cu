@@ -41,7 +41,7 @@ constexpr int kQueue = 16;          // descriptor slots: how far the producer ma
 constexpr int kVMax = 4;            // 16-byte vectors per consumer thread per chunk
 constexpr int kMaxChunkCols = kConsumers * kVMax * 8;   // 8192 bf16 columns = 16 KB per buffer
 constexpr int kMaxBuffers = 64;
-constexpr size_t kSmemBudget = 108 * 1024;   // two CTAs per SM
+constexpr size_t kSmemBudget = 72 * 1024;    // three CTAs per SM
 constexpr uint64_t kWaitNs = 1000000000ull;       // 1 s
 constexpr uint64_t kDrainNs = 50000000ull;        // 50 ms per buffer when draining after a timeout
 
@@ -75,7 +75,7 @@ __host__ __device__ inline size_t gather_smem_bytes(const GatherGeom &g)
 // device word set to 0 before the launch, from which the producers claim
 // their next items (balances skewed source counts).
 template <class Rows, bool WEIGHTED, bool OUT_F32>
-__global__ void __launch_bounds__(kGatherThreads, 2)
+__global__ void __launch_bounds__(kGatherThreads, 3)   // three CTAs per SM: at most 75 registers
 gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows rows, int64_t n_rows,
                   int err_bits, void *__restrict__ out, unsigned int *counter, int32_t *err)
 {
@@ -399,7 +399,7 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
     const int64_t items = T * g.nchunk;
     if (items >= ((int64_t)1 << 30))
         return EP_ERR_UNSUPPORTED;
-    const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), 2 * sm_count());
+    const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), 3 * sm_count());
     if (grid == 0)
         return EP_OK;
     unsigned int *counter = nullptr;
