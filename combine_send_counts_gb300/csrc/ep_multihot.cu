@@ -7,11 +7,16 @@
 //                      +0.0f in ascending k (one slot: its probability).
 //
 // HBM-bound output writes (T*E bytes + 4*T*E bytes) from a small input (12*T*K
-// bytes).  One warp per token: lanes k < K load slot k's id and probability in
-// one coalesced load, the warp broadcasts them by shuffle, and lane l owns the
-// 8 experts [8l, 8l+8) of each 256-expert window, accumulating in registers
-// and writing one 8-byte map store and two 16-byte probability stores, so
-// the warp's stores cover 256 contiguous bytes of map and 1 KB of probs.
+// bytes).  One warp per token.  Lanes k < K hold slot k; __match_any_sync
+// groups the lanes naming the same expert and the lowest lane of each group
+// sums the group's probabilities in ascending slot order (the order of the
+// definition).  Per 256-expert window the warp zeroes a shared-memory row,
+// the group leaders place their sums and hit flags, and each lane writes its 8
+// experts with one 8-byte map store and two 16-byte probability stores, so a
+// warp's stores cover 256 contiguous map bytes and 1 KB of probabilities.
+#include <algorithm>
+#include <climits>
+
 #include "ep_device.cuh"
 #include "ep_internal.h"
 
@@ -20,74 +25,88 @@ namespace {
 
 constexpr int kMultihotThreads = 256;
 constexpr int kMultihotWarps = kMultihotThreads / 32;
+constexpr int kWindow = 256;   // experts per pass: 8 per lane
 
 template <bool VEC>
 __global__ void __launch_bounds__(kMultihotThreads)
 multihot_kernel(const int64_t *__restrict__ idx, const float *__restrict__ p, int64_t T, int K, int E,
                 uint8_t *__restrict__ routing_map, float *__restrict__ probs, int32_t *err)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kMultihotWarps + (threadIdx.x >> 5);
-    if (t >= T)
-        return;   // whole warp
-    int64_t my_id = -1;
-    float my_p = 0.0f;
-    if (lane < K) {
-        my_id = idx[t * K + lane];
-        if (probs != nullptr)   // topk_probs may be NULL for a map-only call
-            my_p = p[t * K + lane];
-    }
-    const bool bad = lane < K && (my_id < -1 || my_id >= E);
-    if (bad)
-        my_id = -1;   // ignored slot
-    if (__any_sync(kFull, bad) && lane == 0)
-        raise(err, EP_ERR_INVALID_EXPERT);
-    for (int w0 = 0; w0 < E; w0 += 256) {
-        const int e0 = w0 + 8 * lane;
-        float acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            acc[j] = 0.0f;
-        uint32_t hit = 0;
-        for (int k = 0; k < K; ++k) {   // ascending k: the sum order
-            const int64_t id = __shfl_sync(kFull, my_id, k);
-            const float pk = __shfl_sync(kFull, my_p, k);
-            const int64_t j = id - e0;
-            if (id >= 0 && j >= 0 && j < 8) {
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)   // static register index
-                    if (jj == j)
-                        acc[jj] = __fadd_rn(acc[jj], pk);
-                hit |= 1u << j;
-            }
+    __shared__ __align__(16) float s_p[kMultihotWarps][kWindow];
+    __shared__ __align__(16) uint8_t s_h[kMultihotWarps][kWindow];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * kMultihotWarps;
+    int64_t t = (int64_t)blockIdx.x * kMultihotWarps + warp;
+    // a token's slots: lane k < K holds slot k (id -1 = masked or ignored)
+    auto load = [&](int64_t tt, int &id, float &pk, bool &bad) {
+        id = -1;
+        pk = 0.0f;
+        bad = false;
+        if (tt < T && lane < K) {
+            const int64_t v = idx[tt * K + lane];
+            bad = v < -1 || v >= E;
+            id = bad ? -1 : (int)v;   // an invalid slot is ignored
+            if (probs != nullptr)     // topk_probs may be NULL for a map-only call
+                pk = p[tt * K + lane];
         }
-        if (e0 >= E)
-            continue;
-        if (VEC) {
-            uint32_t lo = 0, hi = 0;
+    };
+    int id, id_n;
+    float pk, pk_n;
+    bool bad, bad_n;
+    load(t, id, pk, bad);
+    float *sp = s_p[warp];
+    uint8_t *sh = s_h[warp];
+    for (; t < T; t += nw) {
+        load(t + nw, id_n, pk_n, bad_n);   // the warp's next token, if any, loads while this one is written
+        if (__any_sync(kFull, bad) && lane == 0)
+            raise(err, EP_ERR_INVALID_EXPERT);
+        const unsigned peers = __match_any_sync(kFull, id);
+        const bool leader = id >= 0 && (peers & lanemask_lt()) == 0;
+        float sum = 0.0f;   // the group's probabilities, ascending slot order from +0.0f
+        if (id >= 0)
+            for (unsigned m = peers; m != 0; m &= m - 1)
+                sum = __fadd_rn(sum, __shfl_sync(peers, pk, __ffs(m) - 1));
+        for (int w0 = 0; w0 < E; w0 += kWindow) {
+            reinterpret_cast<float4 *>(sp)[2 * lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            reinterpret_cast<float4 *>(sp)[2 * lane + 1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            reinterpret_cast<uint2 *>(sh)[lane] = make_uint2(0u, 0u);
+            __syncwarp();
+            if (leader && id >= w0 && id < w0 + kWindow) {
+                sp[id - w0] = sum;
+                sh[id - w0] = 1;
+            }
+            __syncwarp();
+            const int e0 = w0 + 8 * lane;
+            if (e0 < E) {
+                const float4 a = reinterpret_cast<const float4 *>(sp)[2 * lane];
+                const float4 b = reinterpret_cast<const float4 *>(sp)[2 * lane + 1];
+                const uint2 h = reinterpret_cast<const uint2 *>(sh)[lane];
+                if (VEC) {
+                    if (routing_map != nullptr)
+                        *reinterpret_cast<uint2 *>(routing_map + t * E + e0) = h;
+                    if (probs != nullptr) {
+                        float4 *dst = reinterpret_cast<float4 *>(probs + t * E + e0);
+                        dst[0] = a;
+                        dst[1] = b;
+                    }
+                } else {
+                    const float pv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                lo |= ((hit >> j) & 1u) << (8 * j);
-                hi |= ((hit >> (j + 4)) & 1u) << (8 * j);
+                    for (int j = 0; j < 8; ++j) {
+                        if (e0 + j >= E)
+                            break;
+                        if (routing_map != nullptr)
+                            routing_map[t * E + e0 + j] = sh[8 * lane + j];
+                        if (probs != nullptr)
+                            probs[t * E + e0 + j] = pv[j];
+                    }
+                }
             }
-            if (routing_map != nullptr)
-                *reinterpret_cast<uint2 *>(routing_map + t * E + e0) = make_uint2(lo, hi);
-            if (probs != nullptr) {
-                float4 *dst = reinterpret_cast<float4 *>(probs + t * E + e0);
-                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (e0 + j >= E)
-                    break;
-                if (routing_map != nullptr)
-                    routing_map[t * E + e0 + j] = (uint8_t)((hit >> j) & 1u);
-                if (probs != nullptr)
-                    probs[t * E + e0 + j] = acc[j];
-            }
+            __syncwarp();   // the window is read before the next pass zeroes it
         }
+        id = id_n;
+        pk = pk_n;
+        bad = bad_n;
     }
 }
 
@@ -108,7 +127,10 @@ extern "C" int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk
         return EP_ERR_INVALID_ARG;
     if ((int64_t)T * E >= ((int64_t)1 << 40))
         return EP_ERR_UNSUPPORTED;
-    const int64_t blocks = ceil_div(T, kMultihotWarps);
+    // one warp per token: the hardware keeps more tokens in flight than a
+    // capped grid-stride loop does (measured); the loop covers grids too
+    // large for one launch dimension
+    const int64_t blocks = std::min<int64_t>(ceil_div(T, kMultihotWarps), (int64_t)INT32_MAX);
     const bool vec = E % 8 == 0 && (routing_map == nullptr || aligned(routing_map, 8)) &&
                      (probs == nullptr || aligned(probs, 16));
     if (vec)
