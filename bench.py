@@ -220,30 +220,32 @@ class SendPath:
         self.recv_x = torch.empty((W, w.H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
 
-    def step_nosync(self, y, stream, ev=None, split=False):
+    def step_nosync(self, y, stream, ev=None, split=False, io=None):
         """The no-sync step.  Default: ep_dispatch_nosync (route, then the
         dispatch launched as its programmatic dependent) and ep_combine; ev: 3
         events (start, after route + dispatch, after combine) or None.
         split: ep_route_nosync and ep_dispatch as separate ordinary launches
-        (per-kernel times); ev: 4 events (start, route, dispatch, combine)."""
+        (per-kernel times); ev: 4 events (start, route, dispatch, combine).
+        io: (x, topk_idx, topk_weights, out) to use instead of this path's own."""
         ep, w = self.ep, self.w
         T, K, P, El, H, W = w.T, w.K, w.P, w.E_local, w.H, self.W
+        x, idx, wts, out = io if io is not None else (self.x, self.idx, self.wts, self.out)
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
         rec(0)
         if split:
-            ep.ep_route_nosync(self.idx, self.wts, T, K, P, El, W, self.dest, self.is_in_rank, self.send_counts,
+            ep.ep_route_nosync(idx, wts, T, K, P, El, W, self.dest, self.is_in_rank, self.send_counts,
                                self.rank_offsets, None, self.send_token_idx, self.send_rank, self.send_idx,
                                self.send_w, self.token_pos, self.ws, self.err, stream)
             rec(1)
-            ep.ep_dispatch(self.x, T, H, self.token_pos, P, W, self.recv_x, None, 0, self.err, stream)
+            ep.ep_dispatch(x, T, H, self.token_pos, P, W, self.recv_x, None, 0, self.err, stream)
             rec(2)
         else:
-            ep.ep_dispatch_nosync(self.x, self.idx, self.wts, T, K, H, P, El, W, 0, self.dest, self.is_in_rank,
+            ep.ep_dispatch_nosync(x, idx, wts, T, K, H, P, El, W, 0, self.dest, self.is_in_rank,
                                   self.send_counts, self.rank_offsets, None, self.send_token_idx, self.send_rank,
                                   self.send_idx, self.send_w, self.token_pos, self.recv_x, None, self.ws, self.err,
                                   stream)
             rec(1)
-        ep.ep_combine(y, T, H, self.token_pos, P, W, self.out, 0, self.cws, self.err, stream)
+        ep.ep_combine(y, T, H, self.token_pos, P, W, out, 0, self.cws, self.err, stream)
         rec(3 if split else 2)
 
     def step_sync(self, y, stream, ev=None):
@@ -628,32 +630,66 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
 
 
 def run_e2e(args, ep, torch, w, sp, x_h, idx_h, w_h, y_h, y_dev, stream, world, dist):
-    """The same no-sync step through the C ABI from pinned HOST buffers: H2D of
-    the inputs and of the expert outputs, the path, D2H of the combined
-    result, all inside the timed events."""
+    """The same no-sync step through the C ABI from pinned HOST buffers: every
+    step copies its inputs and expert outputs host -> device, runs the path and
+    copies the combined result device -> host, all inside the timed region.
+    Steps are pipelined over two device buffer sets and three streams (copies
+    in, compute, copies out), so step k+1's uploads overlap step k's compute
+    and download; the timed region runs from the first upload to the last
+    download, and the value is the tokens of all steps over that time."""
+    dev = y_dev.device
     xp, ip, wp, yp = (t.pin_memory() for t in (x_h, idx_h, w_h, y_h))
     outp = torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True)
     N = y_h.shape[0]
     h2d = sum(t.numel() * t.element_size() for t in (xp, ip, wp, yp))
     d2h = outp.numel() * outp.element_size()
-    times = []
-    for k in range(args.e2e_warmup + args.e2e_steps):
+    sets = [(sp.x, sp.idx, sp.wts, y_dev, sp.out)]
+    sets.append((torch.empty_like(sp.x), torch.empty_like(sp.idx), torch.empty_like(sp.wts),
+                 torch.empty_like(y_dev), torch.empty_like(sp.out)))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in sets]
+    ev_c = [torch.cuda.Event() for _ in sets]
+    ev_out = [torch.cuda.Event() for _ in sets]
+
+    def run(steps):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        sp.x.copy_(xp, non_blocking=True)
-        sp.idx.copy_(ip, non_blocking=True)
-        sp.wts.copy_(wp, non_blocking=True)
-        y_dev[:N].copy_(yp, non_blocking=True)
-        sp.step_nosync(y_dev, stream)
-        outp.copy_(sp.out, non_blocking=True)
-        b.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        a.record(s_in)
+        for k in range(steps):
+            j = k % 2
+            x_d, i_d, w_d, y_d, o_d = sets[j]
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_c[j])      # step k-2's compute is done with set j
+                x_d.copy_(xp, non_blocking=True)
+                i_d.copy_(ip, non_blocking=True)
+                w_d.copy_(wp, non_blocking=True)
+                y_d[:N].copy_(yp, non_blocking=True)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            if k >= 2:
+                stream.wait_event(ev_out[j])      # step k-2's download has read out_j
+            sp.step_nosync(y_d, stream, io=(x_d, i_d, w_d, o_d))
+            ev_c[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c[j])
+                outp.copy_(o_d, non_blocking=True)
+                ev_out[j].record(s_out)
+        s_out.wait_stream(stream)
+        b.record(s_out)
         b.synchronize()
-        if k >= args.e2e_warmup:
-            times.append(a.elapsed_time(b) / 1e3)
-    tok_s, _ = aggregate(sum(times), float(w.T * len(times)), world, dist if world > 1 else None)
+        return a.elapsed_time(b) / 1e3
+
+    ref = sp.out.cpu()   # every step has the same inputs: each download must equal the device result
+    run(args.e2e_warmup)
+    total = run(args.e2e_steps)
+    if not torch.equal(outp.view(torch.int16), ref.view(torch.int16)):
+        raise RuntimeError("end-to-end result differs from the device-timed steps' result")
+    tok_s, _ = aggregate(total, float(w.T * args.e2e_steps), world, dist if world > 1 else None)
     return {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": len(times)}
+            "steps": args.e2e_steps, "pipelined": "uploads of step k+1 overlap step k's compute and download"}
 
 
 # ------------------------------------------------------------------ CPU arm --
@@ -726,7 +762,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-other-paths", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--e2e-warmup", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=20, help="oracle steps of the CPU baseline (about 0.5 s each on one core)")
