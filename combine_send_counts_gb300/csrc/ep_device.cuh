@@ -67,6 +67,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Packed fp32 pairs (sm_100 family mul/fma .rn.f32x2): two IEEE
+// round-to-nearest operations in one instruction, each lane's result the same
+// as the scalar __fmul_rn / __fmaf_rn of that lane.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, d;}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// both values rounded to bf16 (RN) and widened back to fp32: one packed
+// conversion, then the two halves of the pair moved into fp32 high halves
+__device__ __forceinline__ float2 round_bf16x2(float2 v)
+{
+    const uint32_t b = pack_bf16x2(v.x, v.y);   // v.x in the low half
+    return make_float2(bf16_lo(b), bf16_hi(b));
+}
+
 }  // namespace ep
 
 namespace ep {

@@ -156,20 +156,56 @@ __device__ __forceinline__ void put_scale(const ScaleSpec &sp, int64_t base, int
 //   power of two: scale = 2^e, the smallest power of two >= a / 448 (from the
 //                 bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
 //                 UE8M0 code e + 127.
+// Group maxima of one chunk.  m[u] is a lane's own maximum over the 8 values
+// of its vector u; a group is vector u of the 16 lanes of one half-warp.  The
+// first log2(U) butterfly steps each hand half of a lane's values to its
+// partner, so that lane l ends with the whole maximum of group
+// u = (l >> 2) & 3 (U = 4) or (l >> 3) & 1 (U = 2) of its half-warp after
+// U + 3 shuffles (instead of 4U).  max is exact, so the order of the steps
+// does not change the value.
+template <int U>
+__device__ __forceinline__ float half_warp_group_max(const float (&m)[U], int lane)
+{
+    static_assert(U == 2 || U == 4, "two or four vectors per lane");
+    float k;
+    if constexpr (U == 4) {
+        const bool b3 = lane & 8, b2 = lane & 4;
+        const float k0 = fmaxf(b3 ? m[2] : m[0], __shfl_xor_sync(kFull, b3 ? m[0] : m[2], 8));
+        const float k1 = fmaxf(b3 ? m[3] : m[1], __shfl_xor_sync(kFull, b3 ? m[1] : m[3], 8));
+        k = fmaxf(b2 ? k1 : k0, __shfl_xor_sync(kFull, b2 ? k0 : k1, 4));
+    } else {
+        const bool b3 = lane & 8;
+        k = fmaxf(b3 ? m[1] : m[0], __shfl_xor_sync(kFull, b3 ? m[0] : m[1], 8));
+        k = fmaxf(k, __shfl_xor_sync(kFull, k, 4));
+    }
+    k = fmaxf(k, __shfl_xor_sync(kFull, k, 2));
+    return fmaxf(k, __shfl_xor_sync(kFull, k, 1));
+}
+
+// the vector u whose group maximum lane l holds after half_warp_group_max
+template <int U>
+__device__ __forceinline__ int group_owner_u(int lane)
+{
+    return U == 4 ? (lane >> 2) & 3 : (lane >> 3) & 1;
+}
+
 // fp8 (1x128) scatter, one warp per token (grid-stride loop over tokens).
 // Lanes j < D (and j + 32) resolve the token's rows; the warp quantises the
 // row once, in chunks of U 16-byte vectors per lane, where lanes 0-15 and
 // 16-31 each hold one 128-element group (group max by half-warp shuffles), and
 // writes each chunk's e4m3 codes and group scales to every row, taking the
-// rows by shuffle.  No shared memory and no block barrier.  With
-// a = max(max|x|, 1e-4):
+// rows by shuffle.  The 2U group maxima of a chunk end up one per lane
+// quad (or octet), so each group's scale is divided out once, by the lane
+// that then stores it, and its reciprocal is handed to the group's lanes by
+// shuffle; a destination row's scale base is computed once per token.  No
+// shared memory and no block barrier.  With a = max(max|x|, 1e-4):
 //   plain (RS = false): q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448;
 //   power of two:       scale = 2^e, the smallest power of two >= a / 448 (from
 //                       the bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
 //                       UE8M0 code e + 127.
 // SF is the scale layout (EP_SCALE_*).
 template <int U, class Rows, int SF, bool RS>
-__global__ void __launch_bounds__(kMoveThreads)
+__global__ void __launch_bounds__(kMoveThreads, 4)
 scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows rows, int64_t n_rows,
                         int err_bits, uint2 *__restrict__ out_q, ScaleSpec sp, int32_t *err)
 {
@@ -179,14 +215,20 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
     const int D = rows.len();
     const int groups = nvec / 16;
     int bad = 0;
+    const int u_own = group_owner_u<U>(lane);                  // this lane's group in a chunk:
+    const int i_own = 32 * u_own + (lane & 16);                 // its first vector from the chunk base
+    const bool owner = (lane & (U == 4 ? 3 : 7)) == 0;          // one lane of the group's owners stores
     for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw) {
         int32_t r_lo = -1, r_hi = -1;
+        int64_t sb_lo = 0, sb_hi = 0;   // scale bases of the rows (column layouts)
         if (lane < D) {
             r_lo = rows.row(t, lane);
             if (r_lo >= n_rows) {
                 bad = err_bits;
                 r_lo = -1;
             }
+            if (SF != EP_SCALE_ROW_F32 && r_lo >= 0)
+                sb_lo = scale_row_base<SF>(sp, r_lo, groups);
         }
         if (lane + 32 < D) {
             r_hi = rows.row(t, lane + 32);
@@ -194,9 +236,13 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
                 bad = err_bits;
                 r_hi = -1;
             }
+            if (SF != EP_SCALE_ROW_F32 && r_hi >= 0)
+                sb_hi = scale_row_base<SF>(sp, r_hi, groups);
         }
         const uint64_t valid =
             (uint64_t)__ballot_sync(kFull, r_lo >= 0) | ((uint64_t)__ballot_sync(kFull, r_hi >= 0) << 32);
+        if (valid == 0)
+            continue;   // warp-uniform: a token with no destination row is not read
         const uint4 *src = x + t * nvec;
         for (int base = 0; base < nvec; base += 32 * U) {
             uint4 vin[U];
@@ -207,56 +253,61 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
                 if (i < nvec)
                     vin[u] = ld_stream(src + i);
             }
+            float m[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {   // vectors past the row are whole half-warps of zeros
+                const uint32_t w[4] = {vin[u].x, vin[u].y, vin[u].z, vin[u].w};
+                m[u] = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    m[u] = fmaxf(m[u], fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+            }
+            // this lane's group: its scale (and UE8M0 code) and the reciprocal
+            const float a = fmaxf(half_warp_group_max<U>(m, lane), 1e-4f);
+            float inv_own, scale_own;
+            uint32_t code_own = 0;
+            if (RS) {
+                const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
+                const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
+                scale_own = __uint_as_float(eb << 23);
+                inv_own = __uint_as_float((254u - eb) << 23);
+                code_own = eb;
+            } else {
+                inv_own = __fdiv_rn(448.0f, a);
+                scale_own = __fdiv_rn(a, 448.0f);
+            }
             uint2 q[U];
-            float scale[U];
-            uint32_t code[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint4 v = vin[u];            // vectors past the row are whole half-warps of zeros
-                float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-                float amax = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    amax = fmaxf(amax, fabsf(f[e]));
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1)
-                    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-                const float a = fmaxf(amax, 1e-4f);
-                float inv;
-                if (RS) {
-                    const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
-                    const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
-                    scale[u] = __uint_as_float(eb << 23);
-                    inv = __uint_as_float((254u - eb) << 23);
-                    code[u] = eb;
-                } else {
-                    inv = __fdiv_rn(448.0f, a);
-                    scale[u] = __fdiv_rn(a, 448.0f);
-                    code[u] = 0;
-                }
+                const float inv = __shfl_sync(kFull, inv_own, (lane & 16) | (U == 4 ? u << 2 : u << 3));
+                const float2 inv2 = make_float2(inv, inv);
+                const uint32_t w[4] = {vin[u].x, vin[u].y, vin[u].z, vin[u].w};
                 uint32_t packed[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 pr = make_float2(__fmul_rn(f[2 * e], inv), __fmul_rn(f[2 * e + 1], inv));
+                    const float2 pr = mul2_rn(make_float2(bf16_lo(w[e]), bf16_hi(w[e])), inv2);
                     packed[e] = (uint32_t)__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
                 }
                 q[u] = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
             }
-            for (uint64_t m = valid; m != 0; m &= m - 1) {   // warp-uniform
-                const int j = __ffsll((long long)m) - 1;
+            const bool put = owner && base + i_own < nvec;
+            for (uint64_t mm = valid; mm != 0; mm &= mm - 1) {   // warp-uniform
+                const int j = __ffsll((long long)mm) - 1;
                 const int32_t r = j < 32 ? __shfl_sync(kFull, r_lo, j) : __shfl_sync(kFull, r_hi, j - 32);
+                int64_t sb;
+                if (SF == EP_SCALE_ROW_F32)
+                    sb = (int64_t)r * groups;
+                else
+                    sb = j < 32 ? __shfl_sync(kFull, sb_lo, j) : __shfl_sync(kFull, sb_hi, j - 32);
                 uint2 *dq = out_q + (int64_t)r * nvec;
-                const int64_t sb = scale_row_base<SF>(sp, r, groups);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int i = base + lane + 32 * u;
-                    if (i < nvec) {
+                    if (i < nvec)
                         st_stream(dq + i, q[u]);
-                        if ((lane & 15) == 0)
-                            put_scale<SF>(sp, sb, i >> 4, scale[u], code[u]);
-                    }
                 }
+                if (put)
+                    put_scale<SF>(sp, sb, (base + i_own) >> 4, scale_own, code_own);
             }
         }
     }
@@ -304,47 +355,10 @@ __global__ void zero_scales_kernel(ScaleSpec sp, const int32_t *__restrict__ fir
 // it converts any, so that enough bytes are in flight to keep HBM busy, and
 // applies the experts one at a time to all 16 values of a vector (16
 // independent fma chains; each value's chain still runs over k ascending).
-// The multiplies and fmas run as sm_100-family packed pairs (mul/fma
-// .rn.f32x2: two IEEE round-to-nearest operations in one instruction, the
-// same results as the scalar forms) and the bf16 rounding of y converts two
-// values per instruction, which cuts the kernel's instruction count by about
-// a third.
+// The multiplies and fmas run as packed pairs (mul2_rn / fma2_rn) and the
+// bf16 rounding of y converts two values per instruction, which cuts the
+// kernel's instruction count by about a third.
 constexpr int kLocalRowsPerBlock = 8;
-
-__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
-{
-    float2 r;
-    asm("{.reg .b64 a, b, d;\n\t"
-        "mov.b64 a, {%2, %3};\n\t"
-        "mov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 d, a, b;\n\t"
-        "mov.b64 {%0, %1}, d;}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-
-__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
-{
-    float2 r;
-    asm("{.reg .b64 a, b, c, d;\n\t"
-        "mov.b64 a, {%2, %3};\n\t"
-        "mov.b64 b, {%4, %5};\n\t"
-        "mov.b64 c, {%6, %7};\n\t"
-        "fma.rn.f32x2 d, a, b, c;\n\t"
-        "mov.b64 {%0, %1}, d;}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
-
-// both values rounded to bf16 (RN) and widened back to fp32: one packed
-// conversion, then the two halves of the pair moved into fp32 high halves
-__device__ __forceinline__ float2 round_bf16x2(float2 v)
-{
-    const uint32_t b = pack_bf16x2(v.x, v.y);   // v.x in the low half
-    return make_float2(bf16_lo(b), bf16_hi(b));
-}
 constexpr int kLocalU = 4;
 
 __global__ void __launch_bounds__(kLocalRowsPerBlock * 32, 4)
