@@ -521,23 +521,26 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
     x = torch.randn((w.T, w.H), device=dev, generator=g).to(torch.bfloat16)
     r = ep.batched_prepare(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, err=err)
     hits = int(r["tokens_per_expert"].sum().item())
+    # tokens with at least one local slot: the only rows a prepare must read
+    t_hit = int((r["slot"] >= 0).any(dim=1).sum().item())
     ws = ep.workspace(w.T, w.K, w.P, w.E_local, 1, dev)
-    ab = (w.T + hits) * w.H * 2
+    ab = (t_hit + hits) * w.H * 2
     us = _event_time_us(torch, flush, lambda: ep.ep_batched_prepare(
         x, idx, w.T, w.K, w.H, w.E, w.E_local, w.rank, w.max_num_tokens, r["b_x"], r["tokens_per_expert"],
         r["slot"], 0, ws, err), iters)
     out["batched_prepare"] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab,
                               "gbs": round(ab / us / 1e3, 1), "frac": round(ab / us / 1e3 / peak, 4),
-                              "local_hits": hits}
+                              "local_hits": hits, "tokens_with_a_local_slot": t_hit}
     y = torch.randn((w.E_local, w.max_num_tokens, w.H), device=dev, generator=g).to(torch.bfloat16)
     o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     us = _event_time_us(torch, flush, lambda: ep.ep_batched_combine(
         y, idx, wts, r["slot"], w.T, w.K, w.H, w.E_local, w.rank, w.max_num_tokens, o, cws, err), iters)
-    out["batched_combine"] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": ab,
-                              "gbs": round(ab / us / 1e3, 1), "frac": round(ab / us / 1e3 / peak, 4)}
+    abc = (w.T + hits) * w.H * 2   # every token's output row is written
+    out["batched_combine"] = {"workload": "batched", "us": round(us, 2), "algorithmic_bytes": abc,
+                              "gbs": round(abc / us / 1e3, 1), "frac": round(abc / us / 1e3 / peak, 4)}
     # fp8 expert-batched prepare: codes + column-major scales (fp32, or
     # power-of-two UE8M0 packed four per int)
-    ab8 = w.T * w.H * 2 + hits * (w.H + w.H // 32)
+    ab8 = t_hit * w.H * 2 + hits * (w.H + w.H // 32)
     for name, fmt, rs in (("batched_prepare_fp8_col_f32", ep.EP_SCALE_COL_F32, 0),
                           ("batched_prepare_fp8_ue8m0", ep.EP_SCALE_COL_UE8M0, 1)):
         r8 = ep.batched_prepare_fp8(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, fmt, bool(rs), err=err)
@@ -551,8 +554,9 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
     # copied, the alignment rows zero-filled
     C = ep.expert_capacity(w.T, w.K, w.E, 1.0)
     rx = ep.batched_prepare_ex(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, capacity=C, alignment=128, err=err)
-    kept = int((rx["tokens_per_expert"]).sum().item())
-    abx = w.T * w.H * 2 + kept * w.H * 2
+    kept = int((rx["tokens_per_expert"]).sum().item())   # kept rows plus alignment rows
+    t_kept = int((rx["slot"] >= 0).any(dim=1).sum().item())
+    abx = t_kept * w.H * 2 + kept * w.H * 2
     us = _event_time_us(torch, flush, lambda: ep.ep_batched_prepare_ex(
         x, idx, w.T, w.K, w.H, w.E, w.E_local, w.rank, w.max_num_tokens, C, 128, rx["b_rows"], None, -1, 0,
         rx["tokens_per_expert"], rx["slot"], rx["dropped"], 0, ws, err), iters)
@@ -598,6 +602,17 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
     out["fp8_dispatch"] = {"workload": f"chunk_fp8, one chunk of {Tc} tokens", "us": round(us, 2),
                            "algorithmic_bytes": ab, "gbs": round(ab / us / 1e3, 1),
                            "frac": round(ab / us / 1e3 / peak, 4), "rows": N}
+    # the synthetic fp8 expert on that chunk's rows: codes + scales + the rows'
+    # expert ids and weights read, bf16 rows written
+    out_l = torch.empty((N, w.H), dtype=torch.bfloat16, device=dev)
+    sidx, sw = rr["send_idx"][:N], rr["send_w"][:N]
+    abl = N * (w.H + w.H // 32 + w.K * 12 + 2 * w.H)
+    us = _event_time_us(torch, flush, lambda: ep.ep_local_expert_fp8(q, sc, sidx, sw, N, w.K, w.H, out_l, err),
+                        iters)
+    out["local_expert_fp8"] = {"workload": f"chunk_fp8, one chunk of {Tc} tokens (the dispatched rows)",
+                               "us": round(us, 2), "algorithmic_bytes": abl, "gbs": round(abl / us / 1e3, 1),
+                               "frac": round(abl / us / 1e3 / peak, 4), "rows": N}
+    del out_l
     us = _event_time_us(torch, flush, lambda: ep.dispatch_chunked_forward(
         x, idx, wts, num_local_experts=w.E_local, num_ranks=w.P, chunks=w.chunks, fp8=True, err=err),
         max(2, iters // 4), warmup=1)
