@@ -11,8 +11,9 @@
 // so the kernel keeps many row loads in flight with the TMA engine rather
 // than with registers:
 //
-//   * two persistent CTAs per SM, each with its own ring; items are (token,
-//     column chunk) pairs, claimed from a shared counter (or dealt round-robin);
+//   * three persistent CTAs per SM, each with its own ring; items are (token,
+//     column chunk) pairs, claimed from a shared counter (or dealt round-robin),
+//     a few at a time and one at a time near the end;
 //   * warp 0 is the producer: it resolves the source lists of 32 items at a
 //     time, publishes each item's descriptor (token, chunk, source count,
 //     weights) in a small queue and issues one 1-D bulk copy
@@ -27,6 +28,7 @@
 // Every wait is bounded (EP_ERR_TIMEOUT after a second); a CTA that gives up
 // waits, again with a bound, for its own copies in flight before it exits.
 #include <algorithm>
+#include <type_traits>
 
 #include "ep_device.cuh"
 #include "ep_internal.h"
@@ -61,6 +63,7 @@ struct GatherGeom {
     int RB;         // bytes per ring buffer (multiple of 128)
     int lpi;        // lanes of the producer warp per item (8, 16 or 32)
     int cb;         // items per claim (32 / lpi)
+    int taper;      // claims from the counter shrink to one item once at most this many items remain (0: never)
 };
 
 __host__ __device__ inline size_t gather_smem_bytes(const GatherGeom &g)
@@ -117,19 +120,29 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
         const int my_i = lane / g.lpi, j0 = lane % g.lpi, j1 = j0 + 32;
         const unsigned item_lanes = (g.lpi == 32 ? kFull : ((1u << g.lpi) - 1u)) << (my_i * g.lpi);
         uint32_t static_k = 0;
-        auto claim = [&]() -> int {
+        // A claim is `count` consecutive items from `base`.  From the shared
+        // counter a CTA takes g.cb items at a time until it sees at most
+        // g.taper items left, then one at a time, so that the CTAs run out of
+        // work at nearly the same time.
+        int seen = 0;   // the counter's value at this CTA's last claim
+        auto claim = [&](int &count) -> int {
+            count = g.cb;
             if (counter == nullptr)
                 return (int)((blockIdx.x + (static_k++) * gridDim.x) * (uint32_t)g.cb);
+            if (n_items - seen <= g.taper)
+                count = 1;
             int c = 0;
             if (lane == 0)
-                c = (int)atomicAdd(counter, (unsigned)g.cb);
-            return __shfl_sync(kFull, c, 0);
+                c = (int)atomicAdd(counter, (unsigned)count);
+            c = __shfl_sync(kFull, c, 0);
+            seen = c;
+            return c;
         };
-        auto load = [&](int base, typename Rows::Raw &r0, typename Rows::Raw &r1, bool &v0, bool &v1) {
+        auto load = [&](int base, int count, typename Rows::Raw &r0, typename Rows::Raw &r1, bool &v0, bool &v1) {
             const int item = base + my_i;
             v0 = false;
             v1 = false;
-            if (item < n_items) {
+            if (my_i < count && item < n_items) {
                 const int64_t t = g.nchunk == 1 ? item : item / g.nchunk;
                 v0 = j0 < D;
                 v1 = j1 < D;
@@ -144,12 +157,13 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
         uint32_t k = 0;    // descriptors published so far
         typename Rows::Raw rc0{}, rc1{}, rn0{}, rn1{};
         bool vc0, vc1, vn0, vn1;
-        int c_cur = claim();
-        int c_nxt = claim();
-        load(c_cur, rc0, rc1, vc0, vc1);
+        int n_cur, n_nxt, n_aft;
+        int c_cur = claim(n_cur);
+        int c_nxt = claim(n_nxt);
+        load(c_cur, n_cur, rc0, rc1, vc0, vc1);
         while (c_cur < n_items && !*abort_flag) {
-            const int c_aft = claim();
-            load(c_nxt, rn0, rn1, vn0, vn1);          // used by the next claim
+            const int c_aft = claim(n_aft);
+            load(c_nxt, n_nxt, rn0, rn1, vn0, vn1);   // used by the next claim
             bool ok = true;
             int32_t r0 = -1, r1 = -1;
             if (vc0) {
@@ -170,7 +184,7 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
             const float w1 = WEIGHTED && vc1 ? rows.weight(rc1) : 1.0f;
             const unsigned bal0 = __ballot_sync(kFull, r0 >= 0);
             const unsigned bal1 = __ballot_sync(kFull, r1 >= 0);
-            for (int i = 0; i < g.cb && ok; ++i) {
+            for (int i = 0; i < n_cur && ok; ++i) {
                 const int item = c_cur + i;
                 if (item >= n_items)
                     break;
@@ -237,6 +251,8 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
             }
             c_cur = c_nxt;
             c_nxt = c_aft;
+            n_cur = n_nxt;
+            n_nxt = n_aft;
             rc0 = rn0;
             rc1 = rn1;
             vc0 = vn0;
@@ -370,6 +386,7 @@ static GatherGeom gather_geometry(int H, int D)
     g.RB = (int)align_up((size_t)g.CH * 2, 128);
     g.lpi = D <= 8 ? 8 : D <= 16 ? 16 : 32;
     g.cb = 32 / g.lpi;
+    g.taper = 0;
     g.B = 0;
     g.logB = 0;
     const size_t fixed = gather_smem_bytes(g);
@@ -385,7 +402,7 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
                              void *out, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream)
 {
     const int D = rows.len();
-    const GatherGeom g = gather_geometry(H, D);
+    GatherGeom g = gather_geometry(H, D);
     const size_t smem = gather_smem_bytes(g);
     auto kernel = gather_tma_kernel<Rows, WEIGHTED, OUT_F32>;
     static size_t smem_set = 0;   // per instantiation; raising the limit is idempotent
@@ -402,6 +419,13 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
     const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), 3 * sm_count());
     if (grid == 0)
         return EP_OK;
+    // One-item claims for the last 4 claims' worth per CTA: a CTA holds up to
+    // three claims ahead when it starts tapering, so a smaller threshold
+    // changes nothing.  On the send layout (about three 14 KB sources per
+    // token) this took the large combine from 141.1 to 138.4 us; the batched
+    // layout's items (about two sources) are too short to hide the row-list
+    // loads of one-item claims (37.6 -> 42.0 us), so it keeps full claims.
+    g.taper = std::is_same<Rows, BatchedRows>::value ? 0 : 4 * grid * g.cb;
     unsigned int *counter = nullptr;
     if (ws != nullptr && ws_bytes >= EP_COMBINE_WS_BYTES) {
         counter = static_cast<unsigned int *>(ws);
