@@ -4,13 +4,16 @@
 //               dispatch; NeMo uccl_ep.buffer, Buffer.dispatch) and the
 //               expert-batched prepare (vLLM BatchedPrepareAndFinalize.prepare):
 //               every source row is read from HBM once and written to each of
-//               its destination rows.
+//               its destination rows, as bf16 or quantised to fp8 (1x128).
+//   zero     -- padding rows (and their scales) of the expert-batched layout.
+//   expert   -- the synthetic fp8 local expert of the chunked forward.
 //   (the combines live in ep_combine.cu)
 //
-// The scatter is an HBM-bound copy.  A group of G threads (a multiple of 32) owns one
-// token; each thread moves U 16-byte vectors of the row, so a row is covered
-// in one pass for H up to 8*G*U.  The destination (or source) row list of the
-// block's tokens is resolved once into shared memory.
+// The bf16 scatter is an HBM-bound copy.  A group of G threads (a multiple of
+// 32) owns one token; each thread moves U 16-byte vectors of the row, so a row
+// is covered in one pass for H up to 8*G*U.  The destination row list of the
+// block's tokens is resolved once into shared memory.  The fp8 scatter gives
+// each token one warp, which also computes the group scales.
 #include <algorithm>
 #include <utility>
 #include <climits>
@@ -149,13 +152,6 @@ __device__ __forceinline__ void put_scale(const ScaleSpec &sp, int64_t base, int
         static_cast<uint8_t *>(sp.out)[base + (int64_t)(gi >> 2) * sp.M * 4 + (gi & 3)] = (uint8_t)code;
 }
 
-// Quantises each source row once, in 128-element groups (16 vectors, held by
-// 16 consecutive lanes because G is a multiple of 32), and writes the e4m3
-// codes and the group scales to each destination row.  With a = max(max|x|, 1e-4):
-//   plain:        q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448;
-//   power of two: scale = 2^e, the smallest power of two >= a / 448 (from the
-//                 bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
-//                 UE8M0 code e + 127.
 // Group maxima of one chunk.  m[u] is a lane's own maximum over the 8 values
 // of its vector u; a group is vector u of the 16 lanes of one half-warp.  The
 // first log2(U) butterfly steps each hand half of a lane's values to its

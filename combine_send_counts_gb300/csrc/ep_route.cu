@@ -7,11 +7,13 @@
 //
 // All three are the same pattern: one thread per token, a warp ballot per
 // destination (rank or local expert) gives each warp's count and every lane's
-// rank among the lanes before it, a shared-memory pass over the block's 8
-// warps gives the block count, and a reduce-then-scan over blocks (partials
-// written to the caller's workspace by one launch, read by the next) gives
-// each block's starting offset.  No atomics decide any position, so every
-// index is deterministic and the order is token-ascending by construction.
+// rank among the lanes before it, a shared-memory pass over the block's warps
+// gives the block count, and a reduce-then-scan over blocks gives each
+// block's starting offset.  The block partials go through the caller's
+// workspace: either from one launch to the next, or, in the single-launch
+// (cooperative) forms, across a bounded grid barrier inside one kernel.  No
+// atomics decide any position, so every index is deterministic and the order
+// is token-ascending by construction.
 #include <algorithm>
 #include <atomic>
 
