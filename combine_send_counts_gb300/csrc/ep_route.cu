@@ -310,6 +310,20 @@ __device__ __forceinline__ void block_rank_sums(const int32_t *__restrict__ part
         atomicAdd(&s_before[p], bef);
 }
 
+// Which layout outputs are aligned for vector stores: the C ABI promises
+// only natural alignment for them, so a wider store is taken only where the
+// caller's pointer allows it (decided on the host, uniform over the launch).
+struct VecOk {
+    bool send_idx;     // 16 bytes: pairs of int64
+    bool send_w;       // 16 bytes: four floats
+    bool is_in_rank;   // 4 bytes: four flags
+};
+
+static VecOk vec_ok(const int64_t *send_idx, const float *send_w, const uint8_t *is_in_rank)
+{
+    return VecOk{aligned(send_idx, 16), aligned(send_w, 16), aligned(is_in_rank, 4)};
+}
+
 // Outputs and mode of layout_write_kernel.
 struct LayoutArgs {
     const int64_t *idx;
@@ -332,12 +346,47 @@ struct LayoutArgs {
     int32_t *token_pos;
     int32_t *err;
     int align;                // rank segments start at multiples of it; tokens_per_expert rounded up
+    VecOk vec;                // which outputs take vector stores
 };
 
+// One token's K-wide send_idx / send_w row for rank p, from the token's ids,
+// weights and owning ranks held in registers (KC = K at compile time).
+template <int KC>
+__device__ __forceinline__ void write_send_row(int64_t *si, float *sw, const int64_t (&id)[KC],
+                                               const float (&wt)[KC], const int8_t (&dr)[KC], int p,
+                                               int64_t off, VecOk vec)
+{
+    if ((KC & 1) == 0 && vec.send_idx) {
+#pragma unroll
+        for (int k = 0; k < KC; k += 2)
+            *reinterpret_cast<longlong2 *>(si + k) =
+                make_longlong2(dr[k] == p ? id[k] - off : -1, dr[k + 1] == p ? id[k + 1] - off : -1);
+    } else {
+#pragma unroll
+        for (int k = 0; k < KC; ++k)
+            si[k] = dr[k] == p ? id[k] - off : -1;
+    }
+    if ((KC & 3) == 0 && vec.send_w) {
+#pragma unroll
+        for (int k = 0; k < KC; k += 4)
+            *reinterpret_cast<float4 *>(sw + k) =
+                make_float4(dr[k] == p ? wt[k] : 0.0f, dr[k + 1] == p ? wt[k + 1] : 0.0f,
+                            dr[k + 2] == p ? wt[k + 2] : 0.0f, dr[k + 3] == p ? wt[k + 3] : 0.0f);
+    } else {
+#pragma unroll
+        for (int k = 0; k < KC; ++k)
+            sw[k] = dr[k] == p ? wt[k] : 0.0f;
+    }
+}
+
 // One block of 256 tokens: the block's first row per rank from the partials,
-// each lane's row from warp ballots, then the rows.  A warp writes the K-wide
-// send_idx / send_w rows of its tokens for one rank together: its rows for
-// rank p are consecutive, so the warp covers them with consecutive stores.
+// each lane's row from warp ballots, then the rows.  KC > 0 (K == KC at
+// compile time): each thread loads its token's K ids, weights and owning
+// ranks once into registers and writes its own rows (vector stores where the
+// outputs are aligned for them).  KC == 0: a warp writes the K-wide send_idx /
+// send_w rows of its tokens for one rank together (its rows for rank p are
+// consecutive), reading each element where it writes it.
+template <int KC>
 __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs a)
 {
     allow_dependents();   // the dispatch after this kernel may start loading its input rows
@@ -437,6 +486,49 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
     __syncthreads();
 
     int bad = 0;
+    if constexpr (KC > 0) {
+        int64_t id[KC];
+        float wt[KC];
+        int8_t dr[KC];
+        uint64_t dmask = 0;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            id[k] = -1;
+            wt[k] = 0.0f;
+            int d = -1;
+            if (valid) {
+                id[k] = a.idx[t * KC + k];
+                wt[k] = a.w[t * KC + k];
+                d = a.dest[t * KC + k];
+            }
+            dr[k] = (int8_t)(d >= 0 && d < P ? d : -1);
+            if (dr[k] >= 0)
+                dmask |= 1ull << d;
+        }
+        if (valid && dmask != mask)
+            bad = EP_ERR_COUNT_MISMATCH;
+        for (int p = 0; p < P; ++p) {
+            const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+            if (!valid)
+                continue;
+            int32_t n = -1;
+            if ((mask >> p) & 1ull) {
+                const int64_t pos = (int64_t)s_base[p] + s_warp[warp][p] + __popc(bal & lanemask_lt());
+                if (pos < a.num_rows) {
+                    n = (int32_t)pos;
+                    a.send_token_idx[n] = (int32_t)t;
+                    a.send_rank[n] = p;
+                    write_send_row<KC>(a.send_idx + pos * KC, a.send_w + pos * KC, id, wt, dr, p,
+                                       (int64_t)p * a.E_local, a.vec);
+                } else {
+                    bad = a.exact ? EP_ERR_COUNT_MISMATCH : EP_ERR_CAPACITY;
+                }
+            }
+            a.token_pos[t * P + p] = n;
+        }
+        raise(a.err, bad);
+        return;
+    }
     if (valid) {
         uint64_t dmask = 0;
         for (int k = 0; k < K; ++k) {
@@ -484,6 +576,17 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
         }
     }
     raise(a.err, bad);
+}
+
+static void launch_layout_write(const LayoutArgs &a, int nb, cudaStream_t stream)
+{
+    switch (a.K) {
+    case 2: layout_write_kernel<2><<<nb, kRouteThreads, 0, stream>>>(a); break;
+    case 4: layout_write_kernel<4><<<nb, kRouteThreads, 0, stream>>>(a); break;
+    case 6: layout_write_kernel<6><<<nb, kRouteThreads, 0, stream>>>(a); break;
+    case 8: layout_write_kernel<8><<<nb, kRouteThreads, 0, stream>>>(a); break;
+    default: layout_write_kernel<0><<<nb, kRouteThreads, 0, stream>>>(a); break;
+    }
 }
 
 // ---------------------------------------------------- expert-batched slots --
@@ -717,6 +820,7 @@ struct FusedArgs {
     GridBarrier bar;
     int align;                // rank segments start at multiples of it; tokens_per_expert rounded up
     int32_t *err;
+    VecOk vec;                // which outputs take vector stores
 };
 
 // KC > 0: K == KC at compile time (vector row stores); KC == 0: any K <= 32.
@@ -816,7 +920,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
             if (k < K)
                 a.dest[t * K + k] = dr[k];
         uint8_t *irow = a.is_in_rank + t * P;
-        if ((P & 3) == 0) {
+        if ((P & 3) == 0 && a.vec.is_in_rank) {
             for (int p = 0; p < P; p += 4)
                 *reinterpret_cast<uint32_t *>(irow + p) =
                     (uint32_t)((mask >> p) & 1ull) | (uint32_t)((mask >> (p + 1)) & 1ull) << 8 |
@@ -911,29 +1015,15 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
         const int64_t off = (int64_t)p * El;
         int64_t *si = a.send_idx + n * K;
         float *sw = a.send_w + n * K;
-        if (KC > 0 && (KC & 1) == 0) {
-#pragma unroll
-            for (int k = 0; k < KM; k += 2) {
-                const longlong2 v = make_longlong2(dr[k] == p ? id[k] - off : -1, dr[k + 1] == p ? id[k + 1] - off : -1);
-                *reinterpret_cast<longlong2 *>(si + k) = v;
-            }
+        if constexpr (KC > 0) {
+            write_send_row<KC>(si, sw, id, wt, dr, p, off, a.vec);
         } else {
 #pragma unroll
             for (int k = 0; k < KM; ++k)
-                if (k < K)
+                if (k < K) {
                     si[k] = dr[k] == p ? id[k] - off : -1;
-        }
-        if (KC > 0 && (KC & 3) == 0) {
-#pragma unroll
-            for (int k = 0; k < KM; k += 4)
-                *reinterpret_cast<float4 *>(sw + k) =
-                    make_float4(dr[k] == p ? wt[k] : 0.0f, dr[k + 1] == p ? wt[k + 1] : 0.0f,
-                                dr[k + 2] == p ? wt[k + 2] : 0.0f, dr[k + 3] == p ? wt[k + 3] : 0.0f);
-        } else {
-#pragma unroll
-            for (int k = 0; k < KM; ++k)
-                if (k < K)
                     sw[k] = dr[k] == p ? wt[k] : 0.0f;
+                }
         }
     }
     raise(a.err, bad);
@@ -1335,8 +1425,9 @@ extern "C" int ep_build_send_layout(const int64_t *topk_idx, const float *topk_w
     if (launch_status() != EP_OK)
         return EP_ERR_CUDA;
     LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_send, 1, part_rank, nb,
-                 nullptr, nullptr, nullptr, nullptr, send_token_idx, send_rank, send_idx, send_w, token_pos, err, 1};
-    layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);
+                 nullptr, nullptr, nullptr, nullptr, send_token_idx, send_rank, send_idx, send_w, token_pos, err, 1,
+                 vec_ok(send_idx, send_w, is_in_rank)};
+    launch_layout_write(a, nb, stream);
     return launch_status();
 }
 
@@ -1377,7 +1468,8 @@ static int route_nosync(const int64_t *topk_idx, const float *topk_weights, int6
     const size_t smem_f = pe != nullptr ? sizeof(int32_t) * E : 0;
     FusedArgs fa{topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
                  rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos,
-                 wl.part_rank, pe, {wl.flags, wl.epoch, next_route_tag()}, align, err};
+                 wl.part_rank, pe, {wl.flags, wl.epoch, next_route_tag()}, align, err,
+                 vec_ok(send_idx, send_w, is_in_rank)};
     bool launched = false;
     int rc;
     switch (K) {
@@ -1405,8 +1497,8 @@ static int route_nosync(const int64_t *topk_idx, const float *topk_weights, int6
         return EP_ERR_CUDA;
     LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_worst_rows, 0, wl.part_rank, nb,
                  pe, send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
-                 token_pos, err, align};
-    layout_write_kernel<<<nb, kRouteThreads, 0, stream>>>(a);
+                 token_pos, err, align, vec_ok(send_idx, send_w, is_in_rank)};
+    launch_layout_write(a, nb, stream);
     return launch_status();
 }
 
