@@ -87,6 +87,7 @@ scatter_bf16_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows row
             v[u] = ld_stream(src + i);
     }
     grid_dependency_wait();
+    allow_dependents();   // a zero fill after this kernel reads only what the kernel before it wrote
     load_lists(rows, T, t0, g.tpb, n_rows, err_bits, s_rows, nullptr, err);
     __syncthreads();
     if (!active)
@@ -206,6 +207,7 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
                         int err_bits, uint2 *__restrict__ out_q, ScaleSpec sp, int32_t *err)
 {
     grid_dependency_wait();
+    allow_dependents();   // a zero fill after this kernel reads only what the kernel before it wrote
     const int lane = threadIdx.x & 31;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int D = rows.len();
@@ -311,11 +313,21 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
 }
 
 // ------------------------------------------------------------- zero padding --
+// The zero fills run after the row scatter as its programmatic dependents: the
+// scatter lets them start once all its blocks have passed their own wait on the
+// slot kernel, so the counts they read (kept and tokens_per_expert, written by
+// the slot kernel) are final, and the rows they write (at or past an expert's
+// kept count) are ones the scatter never writes.  Block (0, 0) of each waits
+// for the kernel before it just before exiting, which is enough for the
+// kernel's completion to imply that one's; the other blocks exit as soon as
+// their rows are written instead of holding their SM slots.
+//
 // Zero rows [first[e], end) of every local expert, end = M when full, else
 // tokens_per_expert[e] (the aligned count); 16-byte stores.
 __global__ void zero_rows_kernel(uint4 *__restrict__ b_x, const int32_t *__restrict__ first,
                                  const int32_t *__restrict__ tokens_per_expert, int full, int M, int nvec)
 {
+    allow_dependents();   // the scale fill after this kernel is independent of it
     const int e = blockIdx.y;
     const int64_t lo = (int64_t)first[e] * nvec;
     const int64_t hi = (int64_t)(full ? M : tokens_per_expert[e]) * nvec;
@@ -323,6 +335,8 @@ __global__ void zero_rows_kernel(uint4 *__restrict__ b_x, const int32_t *__restr
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int64_t i = lo + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi; i += (int64_t)gridDim.x * blockDim.x)
         st_stream(base + i, z);
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        grid_dependency_wait();
 }
 
 // Zero the scale entries of slots [first[e], end) of every local expert (end
@@ -340,6 +354,8 @@ __global__ void zero_scales_kernel(ScaleSpec sp, const int32_t *__restrict__ fir
         const int64_t s = lo + i % (hi - lo), c = i / (hi - lo);
         base[sp.fmt == EP_SCALE_ROW_F32 ? s * per_row + c : c * sp.M + s] = 0u;
     }
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        grid_dependency_wait();
 }
 
 // -------------------------------------------------- synthetic fp8 expert --
@@ -677,15 +693,21 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
         // only the alignment rows (fewer than `alignment`)
         const int64_t zrows = zero_pad ? M : std::min<int64_t>(alignment - 1, M);
         dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(zrows * nvec, 256), 1024)), E_local);
-        zero_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(b_x), kept, tokens_per_expert, zero_pad, M,
-                                                   nvec);
-        if ((rc = launch_status()) != EP_OK)
-            return rc;
+        // dependents of the scatter when there is one (see zero_rows_kernel)
+        const bool dep = T > 0;
+        if (launch_kernel(dep, zero_rows_kernel, grid, dim3(256), 0, stream, static_cast<uint4 *>(b_x),
+                          (const int32_t *)kept, (const int32_t *)tokens_per_expert, zero_pad, M, nvec) != cudaSuccess) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
         if (sp != nullptr) {
             dim3 sgrid((unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(zrows * (H / 128), 256), 256)),
                        E_local);
-            zero_scales_kernel<<<sgrid, 256, 0, stream>>>(*sp, kept, tokens_per_expert, zero_pad, H / 128);
-            return launch_status();
+            if (launch_kernel(dep, zero_scales_kernel, sgrid, dim3(256), 0, stream, *sp, (const int32_t *)kept,
+                              (const int32_t *)tokens_per_expert, zero_pad, H / 128) != cudaSuccess) {
+                cudaGetLastError();
+                return EP_ERR_CUDA;
+            }
         }
     }
     return EP_OK;
