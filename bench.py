@@ -565,6 +565,19 @@ def run_other_paths(ep, torch, wl, dev, flush, peak, iters):
         "algorithmic_bytes": abx, "gbs": round(abx / us / 1e3, 1), "frac": round(abx / us / 1e3 / peak, 4),
         "dropped": int(rx["dropped"].sum().item())}
     del rx
+    # the same with fp8 rows and column-major fp32 scales (kept rows quantised,
+    # alignment rows and their scales zero-filled)
+    rx = ep.batched_prepare_ex(x, idx, w.E, w.E_local, w.rank, w.max_num_tokens, capacity=C, alignment=128,
+                               scale_fmt=ep.EP_SCALE_COL_F32, err=err)
+    abx8 = t_kept * w.H * 2 + kept * (w.H + w.H // 32)
+    us = _event_time_us(torch, flush, lambda: ep.ep_batched_prepare_ex(
+        x, idx, w.T, w.K, w.H, w.E, w.E_local, w.rank, w.max_num_tokens, C, 128, rx["b_rows"], rx["b_scale"],
+        ep.EP_SCALE_COL_F32, 0, rx["tokens_per_expert"], rx["slot"], rx["dropped"], 0, ws, err), iters)
+    out["batched_prepare_fp8_capacity_align"] = {
+        "workload": "batched, fp8 with column-major fp32 scales, capacity factor 1.0, alignment 128",
+        "us": round(us, 2), "algorithmic_bytes": abx8, "gbs": round(abx8 / us / 1e3, 1),
+        "frac": round(abx8 / us / 1e3 / peak, 4)}
+    del rx
     del x, y, o, r
 
     # metadata views of the large workload's routing: multihot map + dense
