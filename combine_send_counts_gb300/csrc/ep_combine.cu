@@ -124,17 +124,26 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
         // counter a CTA takes g.cb items at a time until it sees at most
         // g.taper items left, then one at a time, so that the CTAs run out of
         // work at nearly the same time.
-        int seen = 0;   // the counter's value at this CTA's last claim
-        auto claim = [&](int &count) -> int {
+        // A claim is issued one loop iteration before its value is needed
+        // (claim_issue: lane 0's atomic, or the static index), and taken with
+        // claim_take, so that the producer does not wait for the atomic's
+        // round trip on every claim.
+        int seen = 0;   // the counter's value at this CTA's last claim taken
+        auto claim_issue = [&](int &count) -> int {
             count = g.cb;
             if (counter == nullptr)
                 return (int)((blockIdx.x + (static_k++) * gridDim.x) * (uint32_t)g.cb);
             if (n_items - seen <= g.taper)
                 count = 1;
-            int c = 0;
+            int raw = 0;
             if (lane == 0)
-                c = (int)atomicAdd(counter, (unsigned)count);
-            c = __shfl_sync(kFull, c, 0);
+                raw = (int)atomicAdd(counter, (unsigned)count);
+            return raw;
+        };
+        auto claim_take = [&](int raw) -> int {
+            if (counter == nullptr)
+                return raw;
+            const int c = __shfl_sync(kFull, raw, 0);
             seen = c;
             return c;
         };
@@ -158,11 +167,11 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
         typename Rows::Raw rc0{}, rc1{}, rn0{}, rn1{};
         bool vc0, vc1, vn0, vn1;
         int n_cur, n_nxt, n_aft;
-        int c_cur = claim(n_cur);
-        int c_nxt = claim(n_nxt);
+        int c_cur = claim_take(claim_issue(n_cur));
+        int c_nxt = claim_take(claim_issue(n_nxt));
+        int raw_aft = claim_issue(n_aft);   // in flight during the first iteration
         load(c_cur, n_cur, rc0, rc1, vc0, vc1);
         while (c_cur < n_items && !*abort_flag) {
-            const int c_aft = claim(n_aft);
             load(c_nxt, n_nxt, rn0, rn1, vn0, vn1);   // used by the next claim
             bool ok = true;
             int32_t r0 = -1, r1 = -1;
@@ -250,9 +259,10 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
                 break;
             }
             c_cur = c_nxt;
-            c_nxt = c_aft;
+            c_nxt = claim_take(raw_aft);
             n_cur = n_nxt;
             n_nxt = n_aft;
+            raw_aft = claim_issue(n_aft);
             rc0 = rn0;
             rc1 = rn1;
             vc0 = vn0;
