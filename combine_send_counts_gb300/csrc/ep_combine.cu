@@ -46,6 +46,8 @@ constexpr int kMaxBuffers = 64;
 constexpr size_t kSmemBudget = 72 * 1024;    // three CTAs per SM
 constexpr uint64_t kWaitNs = 1000000000ull;       // 1 s
 constexpr uint64_t kDrainNs = 50000000ull;        // 50 ms per buffer when draining after a timeout
+constexpr int kSendTaper = 4;      // claims per CTA left when the send layout's claims shrink to one item
+constexpr int kBatchedTaper = 2;   // the same on the batched layout
 
 struct Desc {
     int64_t t;
@@ -429,13 +431,12 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
     const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), 3 * sm_count());
     if (grid == 0)
         return EP_OK;
-    // One-item claims for the last 4 claims' worth per CTA: a CTA holds up to
-    // three claims ahead when it starts tapering, so a smaller threshold
-    // changes nothing.  On the send layout (about three 14 KB sources per
-    // token) this took the large combine from 141.1 to 138.4 us; the batched
-    // layout's items (about two sources) are too short to hide the row-list
-    // loads of one-item claims (37.6 -> 42.0 us), so it keeps full claims.
-    g.taper = std::is_same<Rows, BatchedRows>::value ? 0 : 4 * grid * g.cb;
+    // One-item claims for the last few claims' worth per CTA (thresholds
+    // measured: on the send layout, about three 14 KB sources per token, 4
+    // claims took the large combine from 141.1 to 138.4 us, 2 and 3 were
+    // slower; on the batched layout, about two 8 KB sources per token, 2
+    // claims took it from 35.5 to 33.9 us, 4 and 6 were slower).
+    g.taper = (std::is_same<Rows, BatchedRows>::value ? kBatchedTaper : kSendTaper) * grid * g.cb;
     unsigned int *counter = nullptr;
     if (ws != nullptr && ws_bytes >= EP_COMBINE_WS_BYTES) {
         counter = static_cast<unsigned int *>(ws);
