@@ -27,8 +27,13 @@
  *   - Errors found on the device are OR-ed into *err (a device int32 the
  *     caller zeroes and reads after synchronising; may be NULL).  A kernel that
  *     finds a bad element skips it and never writes out of bounds.
- *   - Matrices are row-major and contiguous.  bf16 rows (x, y, recv_x, out)
- *     must start 16-byte aligned and H must be a multiple of 8.
+ *   - Matrices are row-major and contiguous.  Row matrices of hidden
+ *     vectors (bf16 or fp8 rows: x, y, recv_x, b_x, out and their fp8 forms)
+ *     must start 16-byte aligned and H must be a multiple of 8 (the calls
+ *     return EP_ERR_INVALID_ARG otherwise); workspaces have their own rule
+ *     below.  Every other array (ids, weights, counts, layouts, flags, scales,
+ *     multihot outputs) needs only its element type's natural alignment:
+ *     wider stores are used only where a pointer allows them.
  *   - Token, row and count indices are int32 (T * min(K,P) < 2^31); expert ids
  *     are int64 with -1 meaning "unrouted" ([AX] dispatch, [UB]
  *     get_dispatch_layout).
