@@ -8,12 +8,26 @@ the current CUDA stream is passed through, and a non-OK status raises
 CPU or PyTorch fallback, and using the binding without the built library on a
 CUDA device raises.
 
-The lower-case helpers at the end (``compute_send_counts``,
-``build_send_layout``, ``dispatch``, ``combine``, ``batched_prepare``,
-``batched_combine``, ``chunk_bounds``) allocate outputs with torch and call
-the ``ep_*`` entry points; they follow the call shapes of the axolotl
-``integrations.expert_parallel.torch_dispatch`` page and the vLLM
-``BatchedPrepareAndFinalize`` page.
+The lower-case helpers after them allocate outputs with torch and call the
+``ep_*`` entry points:
+
+- send layout, following the axolotl ``integrations.expert_parallel.
+  torch_dispatch`` page: ``compute_send_counts``, ``build_send_layout``,
+  ``dispatch`` / ``combine`` (the host-synchronising call order),
+  ``route_nosync`` (worst-case rows, no host round trip), ``dispatch_rows``,
+  ``combine_rows``, ``chunk_bounds``, ``dispatch_chunked_forward``,
+  ``dispatch_chunked_forward_nosync`` and ``ChunkedForward`` (buffers kept for
+  repeated or graph-captured calls), ``local_expert_fp8`` (the synthetic
+  expert of the chunked fp8 workload);
+- expert-batched layout, following the vLLM ``BatchedPrepareAndFinalize``
+  page and the NeMo ``uccl_ep.buffer`` low-latency calls:
+  ``batched_prepare``, ``batched_prepare_fp8`` (scale layouts),
+  ``batched_prepare_ex`` (capacity and alignment, NeMo token-dispatcher
+  options), ``expert_capacity``, ``batched_combine``;
+- ``indices_to_multihot``: the NeMo token dispatchers' routing map and dense
+  probabilities;
+- ``workspace``, ``combine_ws``, ``error_word``: scratch and the device error
+  word, allocated the way the entry points expect.
 """
 from __future__ import annotations
 
