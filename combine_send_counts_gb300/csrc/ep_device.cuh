@@ -180,6 +180,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     return true;
 }
 
+// Ask the L2 to fetch [src, src + bytes) (a hint; no data is returned).
+// src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk copy global -> shared (the TMA engine), completing `bytes` of
 // transaction count on `bar`.  Both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)

@@ -47,11 +47,22 @@ struct SlotLimits {
     int32_t *kept;      // [E_local] tokens kept per expert, or null
 };
 
+// Rows that a routing kernel asks the L2 to fetch while its blocks wait for
+// one another, for the kernel that moves them next: the rows t < tokens of
+// x (row_bytes each, 16-byte aligned) that have a destination.  x == nullptr:
+// none.
+struct RowPrefetch {
+    const void *x;
+    int64_t row_bytes;
+    int64_t tokens;
+};
+
 // Launchers implemented in ep_route.cu and used by the batched entry points.
 // The workspace [ws, ws + ws_bytes) is theirs.
 int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
                          const SlotLimits &lim, int32_t *tokens_per_expert, int32_t *slot,
-                         void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream);
+                         void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream,
+                         const RowPrefetch &pf = RowPrefetch{});
 
 // ep_dispatch (ep_move.cu); dependent = launch the scatter as a programmatic
 // dependent of the kernel the library enqueued just before it.

@@ -488,6 +488,20 @@ static cudaError_t launch_kernel(bool dependent, void (*kernel)(KArgs...), dim3 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+static int64_t l2_bytes()
+{
+    static int bytes = -1;
+    if (bytes < 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+            cudaGetLastError();
+            v = 0;
+        }
+        bytes = v;
+    }
+    return bytes;
+}
+
 static int device_sms()
 {
     static int sms = 0;
@@ -673,8 +687,12 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
     int32_t *kept = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + slot_ws);
 
     const SlotLimits lim{M, capacity > 0 ? capacity : M, capacity > 0, alignment, dropped, kept};
+    // the slot kernel brings the rows the scatter reads into the L2 (up to
+    // three quarters of it) while its blocks wait for one another
+    const int64_t row_bytes = (int64_t)H * 2;
+    const RowPrefetch pf{x, row_bytes, std::min<int64_t>(T, l2_bytes() / 4 * 3 / row_bytes)};
     int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, lim, tokens_per_expert, slot, ws, slot_ws,
-                                  err, stream);
+                                  err, stream, pf);
     if (rc != EP_OK)
         return rc;
     if (T > 0) {

@@ -590,6 +590,7 @@ static void launch_layout_write(const LayoutArgs &a, int nb, cudaStream_t stream
 }
 
 // ---------------------------------------------------- expert-batched slots --
+constexpr bool kBatchedPrefetch = true;
 // Local experts are handled 64 at a time (one ballot per expert of the group).
 constexpr int kGroup = 64;
 
@@ -1088,6 +1089,7 @@ struct BatchedFusedArgs {
     int32_t *part;                    // [gridDim][E_local]
     GridBarrier bar;
     int32_t *err;
+    RowPrefetch pf;                   // rows for the scatter after this kernel
 };
 
 template <int KC>
@@ -1158,6 +1160,11 @@ __global__ void __launch_bounds__(kFusedThreads) batched_fused_kernel(BatchedFus
     __syncthreads();
     if (threadIdx.x == 0)
         barrier_arrive(a.bar, s_tag);
+    // HBM is otherwise idle while the blocks wait for one another: the rows
+    // the scatter after this kernel reads (tokens with a local slot) are
+    // fetched into the L2 now
+    if (kBatchedPrefetch && a.pf.x != nullptr && mask != 0 && t < a.pf.tokens)
+        prefetch_l2_bulk(static_cast<const uint8_t *>(a.pf.x) + t * a.pf.row_bytes, (uint32_t)a.pf.row_bytes);
     if (!barrier_wait(a.bar, s_tag, s_epoch, &s_fail)) {
         if (threadIdx.x == 0)
             raise(a.err, EP_ERR_TIMEOUT);
@@ -1238,7 +1245,7 @@ static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t 
 
 int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
                          const SlotLimits &lim, int32_t *tokens_per_expert, int32_t *slot,
-                         void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream)
+                         void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream, const RowPrefetch &pf)
 {
     const int64_t e0 = (int64_t)rank * E_local;
     if (T == 0) {   // every expert receives nothing
@@ -1258,7 +1265,7 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
                             reinterpret_cast<int32_t *>(wsb + kWsAlign),
                             {reinterpret_cast<unsigned long long *>(wsb + kWsAlign + part_bytes),
                              reinterpret_cast<unsigned long long *>(wsb), next_route_tag()},
-                            err};
+                            err, pf};
         bool launched = false;
         int rc;
         switch (K) {
