@@ -687,10 +687,12 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
     int32_t *kept = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + slot_ws);
 
     const SlotLimits lim{M, capacity > 0 ? capacity : M, capacity > 0, alignment, dropped, kept};
-    // the slot kernel brings the rows the scatter reads into the L2 (up to
-    // three quarters of it) while its blocks wait for one another
+    // the slot kernel brings the rows the bf16 scatter reads into the L2 (up
+    // to three quarters of it) while its blocks wait for one another; the fp8
+    // scatter is bound by its arithmetic, not its reads, and gains nothing
     const int64_t row_bytes = (int64_t)H * 2;
-    const RowPrefetch pf{x, row_bytes, std::min<int64_t>(T, l2_bytes() / 4 * 3 / row_bytes)};
+    const RowPrefetch pf{sp == nullptr ? x : nullptr, row_bytes,
+                         std::min<int64_t>(T, l2_bytes() / 4 * 3 / row_bytes)};
     int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, lim, tokens_per_expert, slot, ws, slot_ws,
                                   err, stream, pf);
     if (rc != EP_OK)
