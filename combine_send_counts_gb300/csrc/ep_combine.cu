@@ -28,6 +28,7 @@
 // Every wait is bounded (EP_ERR_TIMEOUT after a second); a CTA that gives up
 // waits, again with a bound, for its own copies in flight before it exits.
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "ep_device.cuh"
@@ -378,17 +379,6 @@ gather_tma_kernel(const uint8_t *__restrict__ y, int64_t T, GatherGeom g, Rows r
 }
 
 // ------------------------------------------------------------ launch policy --
-static int sm_count()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 148;
-    }
-    return n;
-}
-
 static GatherGeom gather_geometry(int H, int D)
 {
     GatherGeom g;
@@ -417,18 +407,18 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
     GatherGeom g = gather_geometry(H, D);
     const size_t smem = gather_smem_bytes(g);
     auto kernel = gather_tma_kernel<Rows, WEIGHTED, OUT_F32>;
-    static size_t smem_set = 0;   // per instantiation; raising the limit is idempotent
-    if (smem > smem_set) {
+    static std::atomic<size_t> smem_set{0};   // per instantiation; raising the limit is idempotent
+    if (smem > smem_set.load(std::memory_order_relaxed)) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
             cudaGetLastError();
             return EP_ERR_CUDA;
         }
-        smem_set = smem;
+        smem_set.store(smem, std::memory_order_relaxed);
     }
     const int64_t items = T * g.nchunk;
     if (items >= ((int64_t)1 << 30))
         return EP_ERR_UNSUPPORTED;
-    const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), 3 * sm_count());
+    const int grid = (int)std::min<int64_t>(ceil_div(items, g.cb), 3 * device_sm_count());
     if (grid == 0)
         return EP_OK;
     // One-item claims for the last few claims' worth per CTA (thresholds

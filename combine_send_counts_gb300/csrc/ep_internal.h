@@ -22,6 +22,11 @@ inline int launch_status()
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
+// Attributes of the current device, read on first use and kept (the library
+// runs on one kind of GPU; concurrent first calls may both read them).
+int device_sm_count();        // streaming multiprocessors (152 if unreadable)
+int64_t device_l2_bytes();    // L2 cache size in bytes (0 if unreadable)
+
 // Upper bound on routing blocks for T tokens split into `chunks` ranges.
 inline int64_t route_blocks_max(int64_t T, int chunks)
 {

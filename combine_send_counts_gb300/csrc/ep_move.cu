@@ -15,6 +15,7 @@
 // block's tokens is resolved once into shared memory.  The fp8 scatter gives
 // each token one warp, which also computes the group scales.
 #include <algorithm>
+#include <atomic>
 #include <utility>
 #include <climits>
 
@@ -488,31 +489,36 @@ static cudaError_t launch_kernel(bool dependent, void (*kernel)(KArgs...), dim3 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-static int64_t l2_bytes()
+static int device_attribute(cudaDeviceAttr attr, int fallback)
 {
-    static int bytes = -1;
-    if (bytes < 0) {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
-            cudaGetLastError();
-            v = 0;
-        }
-        bytes = v;
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fallback;
     }
-    return bytes;
+    return v;
 }
 
-static int device_sms()
+int device_sm_count()
 {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            sms = 152;
-        }
+    static std::atomic<int> sms{0};
+    int v = sms.load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = device_attribute(cudaDevAttrMultiProcessorCount, 152);
+        sms.store(v, std::memory_order_relaxed);
     }
-    return sms;
+    return v;
+}
+
+int64_t device_l2_bytes()
+{
+    static std::atomic<int> bytes{-1};
+    int v = bytes.load(std::memory_order_relaxed);
+    if (v < 0) {
+        v = device_attribute(cudaDevAttrL2CacheSize, 0);
+        bytes.store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 template <class Rows>
@@ -549,7 +555,7 @@ static int launch_scatter_fp8_as(const void *x, int64_t T, int H, const Rows &ro
 {
     const int nvec = H / 8;
     const int64_t warps = kMoveThreads / 32;
-    const int64_t blocks = std::min<int64_t>(ceil_div(T, warps), (int64_t)8 * device_sms());
+    const int64_t blocks = std::min<int64_t>(ceil_div(T, warps), (int64_t)8 * device_sm_count());
     if (blocks == 0)
         return EP_OK;
     auto *xs = static_cast<const uint4 *>(x);
@@ -692,7 +698,7 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
     // scatter is bound by its arithmetic, not its reads, and gains nothing
     const int64_t row_bytes = (int64_t)H * 2;
     const RowPrefetch pf{sp == nullptr ? x : nullptr, row_bytes,
-                         std::min<int64_t>(T, l2_bytes() / 4 * 3 / row_bytes)};
+                         std::min<int64_t>(T, device_l2_bytes() / 4 * 3 / row_bytes)};
     int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, lim, tokens_per_expert, slot, ws, slot_ws,
                                   err, stream, pf);
     if (rc != EP_OK)

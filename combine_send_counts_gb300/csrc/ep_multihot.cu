@@ -16,6 +16,7 @@
 // experts with one 8-byte map store and two 16-byte probability stores, so a
 // warp's stores cover 256 contiguous map bytes and 1 KB of probabilities.
 #include <algorithm>
+#include <atomic>
 
 #include "ep_device.cuh"
 #include "ep_internal.h"
@@ -133,8 +134,8 @@ extern "C" int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk
     // the next token's slots loaded ahead: on 32 K tokens this beat one warp
     // per token (16.3 -> 14.3 us; the same at 16 K tokens), since short-lived
     // blocks pay their scheduling in every wave
-    static int resident[2] = {0, 0};   // blocks per SM, [vec]
-    int &per_sm = resident[vec ? 1 : 0];
+    static std::atomic<int> resident[2] = {{0}, {0}};   // blocks per SM, [vec]
+    int per_sm = resident[vec ? 1 : 0].load(std::memory_order_relaxed);
     if (per_sm == 0) {
         int n = 0;
         const cudaError_t e = vec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, multihot_kernel<true>,
@@ -146,13 +147,9 @@ extern "C" int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk
             n = 4;
         }
         per_sm = std::max(n, 1);
+        resident[vec ? 1 : 0].store(per_sm, std::memory_order_relaxed);
     }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        sms = 152;
-    }
-    const int64_t blocks = std::min<int64_t>(ceil_div(T, kMultihotWarps), (int64_t)per_sm * sms);
+    const int64_t blocks = std::min<int64_t>(ceil_div(T, kMultihotWarps), (int64_t)per_sm * device_sm_count());
     if (vec)
         multihot_kernel<true><<<blocks, kMultihotThreads, 0, stream>>>(topk_idx, topk_probs, T, K, E, routing_map,
                                                                        probs, err);

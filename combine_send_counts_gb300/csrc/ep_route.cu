@@ -960,22 +960,21 @@ template <int KC>
 static int launch_route_fused(const FusedArgs &a, int nb, size_t smem, cudaStream_t stream, bool *launched)
 {
     *launched = false;
-    static int max_per_sm[2] = {-1, -1};   // [counting experts?]
+    // blocks per SM, [counting experts?]; with dynamic shared memory the
+    // count depends on smem, which a call with expert counts passes as E ints
+    static std::atomic<int> max_per_sm[2] = {{-1}, {-1}};
     const int slot = smem > 0 ? 1 : 0;
-    if (max_per_sm[slot] < 0) {
+    int per_sm = max_per_sm[slot].load(std::memory_order_relaxed);
+    if (per_sm < 0 || slot == 1) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_fused_kernel<KC>, kFusedThreads, smem) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
-        max_per_sm[slot] = n;
+        per_sm = n;
+        max_per_sm[slot].store(n, std::memory_order_relaxed);
     }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return EP_OK;
-    }
-    if ((int64_t)max_per_sm[slot] * sms < nb)
+    if ((int64_t)per_sm * device_sm_count() < nb)
         return EP_OK;   // cannot be co-resident: the caller falls back to two launches
     FusedArgs copy = a;
     void *args[] = {&copy};
@@ -1142,21 +1141,19 @@ template <int KC>
 static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t stream, bool *launched)
 {
     *launched = false;
-    static int max_per_sm = -1;
-    if (max_per_sm < 0) {
+    static std::atomic<int> max_per_sm{-1};
+    int per_sm = max_per_sm.load(std::memory_order_relaxed);
+    if (per_sm < 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, batched_fused_kernel<KC>, kFusedThreads, 0) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
-        max_per_sm = n;
+        per_sm = n;
+        max_per_sm.store(n, std::memory_order_relaxed);
     }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return EP_OK;
-    }
-    if ((int64_t)max_per_sm * sms < nb)
+    const int sms = device_sm_count();
+    if ((int64_t)per_sm * sms < nb)
         return EP_OK;
     BatchedFusedArgs copy = a;
     void *args[] = {&copy};
