@@ -182,6 +182,18 @@ def _check(rc: int, where: str):
         raise EPError(rc, where)
 
 
+def _expect(where: str, **tensors):
+    """dtype checks of the allocating helpers: name=(tensor, dtype or tuple of
+    dtypes); None tensors are skipped.  The C ABI takes untyped pointers, so a
+    tensor of the wrong type would otherwise be read as the expected one."""
+    for name, (t, dt) in tensors.items():
+        if t is None:
+            continue
+        want = dt if isinstance(dt, tuple) else (dt,)
+        if t.dtype not in want:
+            raise TypeError(f"{where}: {name} must be {' or '.join(str(d) for d in want)}, got {t.dtype}")
+
+
 # ------------------------------------------------------------- C ABI names --
 def ep_status_str(status: int) -> str:
     return load().ep_status_str(int(status)).decode()
@@ -360,6 +372,7 @@ def compute_send_counts(topk_idx: torch.Tensor, num_ranks: int, num_local_expert
                         chunk_bounds: Optional[Sequence[int]] = None, ws=None, err=None, stream=None,
                         with_tokens_per_expert: bool = True):
     """-> dict(dest, is_in_rank, send_counts [C,P], rank_offsets [C,P+1], tokens_per_expert)."""
+    _expect("compute_send_counts", topk_idx=(topk_idx, torch.int64))
     T, K = topk_idx.shape
     P, El = num_ranks, num_local_experts
     C = len(chunk_bounds) - 1 if chunk_bounds is not None else 1
@@ -383,6 +396,8 @@ def compute_send_counts(topk_idx: torch.Tensor, num_ranks: int, num_local_expert
 def build_send_layout(topk_idx, topk_weights, dest, is_in_rank, num_send: int, num_local_experts: int,
                       ws=None, err=None, stream=None):
     """-> dict(send_token_idx [N], send_rank [N], send_idx [N,K], send_w [N,K], token_pos [T,P])."""
+    _expect("build_send_layout", topk_idx=(topk_idx, torch.int64), topk_weights=(topk_weights, torch.float32),
+            dest=(dest, torch.int32), is_in_rank=(is_in_rank, torch.uint8))
     T, K = topk_idx.shape
     P = is_in_rank.shape[1]
     dev = topk_idx.device
@@ -409,6 +424,7 @@ def route_nosync(topk_idx, topk_weights, num_ranks: int, num_local_experts: int,
     (no host round trip).  rank_offsets[P] holds the number of rows used.
     alignment > 1 starts every rank segment at a multiple of it (pad rows
     carry no token) and rounds tokens_per_expert up."""
+    _expect("route_nosync", topk_idx=(topk_idx, torch.int64), topk_weights=(topk_weights, torch.float32))
     T, K = topk_idx.shape
     P, El = num_ranks, num_local_experts
     W = T * min(K, P) + P * (alignment - 1) if num_worst_rows is None else int(num_worst_rows)
@@ -438,6 +454,7 @@ def route_nosync(topk_idx, topk_weights, num_ranks: int, num_local_experts: int,
 def dispatch_rows(x: torch.Tensor, token_pos: torch.Tensor, num_send: int, fp8: bool = False, err=None,
                   stream=None):
     """recv_x [N,H] bf16, or (recv_q [N,H] e4m3 as uint8, recv_scale [N,H/128] fp32) when fp8."""
+    _expect("dispatch_rows", x=(x, torch.bfloat16), token_pos=(token_pos, torch.int32))
     T, H = x.shape
     P = token_pos.shape[1]
     err = err if err is not None else error_word(x.device)
@@ -462,6 +479,7 @@ def combine_ws(device=None) -> torch.Tensor:
 def combine_rows(y: torch.Tensor, token_pos: torch.Tensor, out_dtype=torch.bfloat16, err=None, stream=None,
                  ws="auto"):
     """ws: "auto" (a fresh scratch), a device tensor, or None (static work split)."""
+    _expect("combine_rows", y=(y, torch.bfloat16), token_pos=(token_pos, torch.int32))
     T, P = token_pos.shape
     N, H = y.shape
     out = torch.empty((T, H), dtype=out_dtype, device=y.device)
@@ -491,6 +509,7 @@ def combine(local_out: torch.Tensor, handle: dict, dtype=None):
 def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int,
                     zero_pad: bool = False, err=None, stream=None):
     """-> dict(b_x [E_local,M,H], tokens_per_expert [E_local], slot [T,K])."""
+    _expect("batched_prepare", x=(x, torch.bfloat16), topk_idx=(topk_idx, torch.int64))
     T, H = x.shape
     K = topk_idx.shape[1]
     El = num_local_experts
@@ -535,6 +554,7 @@ def ep_indices_to_multihot(topk_idx, topk_probs, T, K, E, routing_map, probs, er
 
 def indices_to_multihot(topk_idx, topk_probs, num_experts: int, err=None, stream=None):
     """-> (routing_map [T,E] bool, probs [T,E] fp32): the multihot view of top-k routing."""
+    _expect("indices_to_multihot", topk_idx=(topk_idx, torch.int64), topk_probs=(topk_probs, torch.float32))
     T, K = topk_idx.shape
     dev = topk_idx.device
     rm = torch.empty((T, num_experts), dtype=torch.bool, device=dev)
@@ -563,6 +583,7 @@ def batched_prepare_ex(x, topk_idx, num_experts: int, num_local_experts: int, ra
     overflow is an error; else later tokens are dropped and counted) and a
     receive alignment.  scale_fmt None: bf16 rows; else fp8 codes + scales.
     -> dict(b_rows, b_scale, tokens_per_expert, slot, dropped, err)."""
+    _expect("batched_prepare_ex", x=(x, torch.bfloat16), topk_idx=(topk_idx, torch.int64))
     T, H = x.shape
     K = topk_idx.shape[1]
     El, M = num_local_experts, max_num_tokens
@@ -600,6 +621,7 @@ def batched_prepare_fp8(x, topk_idx, num_experts: int, num_local_experts: int, r
                         err=None, stream=None):
     """-> dict(b_q [E_local,M,H] uint8 (e4m3 codes), b_scale (batched_scale_storage),
     tokens_per_expert [E_local], slot [T,K])."""
+    _expect("batched_prepare_fp8", x=(x, torch.bfloat16), topk_idx=(topk_idx, torch.int64))
     T, H = x.shape
     K = topk_idx.shape[1]
     El = num_local_experts
@@ -617,6 +639,8 @@ def batched_prepare_fp8(x, topk_idx, num_experts: int, num_local_experts: int, r
 
 
 def batched_combine(y, topk_idx, topk_weights, slot, rank: int, err=None, stream=None, ws="auto"):
+    _expect("batched_combine", y=(y, torch.bfloat16), topk_idx=(topk_idx, torch.int64),
+            topk_weights=(topk_weights, torch.float32), slot=(slot, torch.int32))
     El, M, H = y.shape
     T, K = topk_idx.shape
     out = torch.empty((T, H), dtype=y.dtype, device=y.device)
@@ -627,6 +651,8 @@ def batched_combine(y, topk_idx, topk_weights, slot, rank: int, err=None, stream
 
 
 def local_expert_fp8(recv_q, recv_scale, send_idx, send_w, err=None, stream=None):
+    _expect("local_expert_fp8", recv_q=(recv_q, (torch.uint8, torch.float8_e4m3fn)), recv_scale=(recv_scale, torch.float32),
+            send_idx=(send_idx, torch.int64), send_w=(send_w, torch.float32))
     N, H = recv_q.shape
     K = send_idx.shape[1]
     out = torch.empty((N, H), dtype=torch.bfloat16, device=recv_q.device)

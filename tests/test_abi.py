@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import combine_send_counts_gb300 as ep
 from combine_send_counts_gb300 import _build
@@ -128,3 +129,22 @@ def test_ctypes_structs_match_the_header(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for f, _ in cls._fields_:
             assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
+
+
+def test_helpers_reject_wrong_dtypes_before_any_device_work():
+    # the C ABI takes untyped pointers; the allocating helpers check the dtypes
+    # first, so these fail on the host (CPU tensors, no CUDA needed)
+    x32 = torch.zeros((4, 8), dtype=torch.float32)
+    idx = torch.zeros((4, 2), dtype=torch.int64)
+    w = torch.zeros((4, 2), dtype=torch.float32)
+    tp = torch.zeros((4, 2), dtype=torch.int32)
+    with pytest.raises(TypeError, match="x must be torch.bfloat16"):
+        ep.dispatch_rows(x32, tp, 4)
+    with pytest.raises(TypeError, match="topk_idx must be torch.int64"):
+        ep.compute_send_counts(idx.to(torch.int32), 2, 2)
+    with pytest.raises(TypeError, match="topk_weights must be torch.float32"):
+        ep.route_nosync(idx, w.to(torch.float64), 2, 2)
+    with pytest.raises(TypeError, match="y must be torch.bfloat16"):
+        ep.combine_rows(x32, tp)
+    with pytest.raises(TypeError, match="slot must be torch.int32"):
+        ep.batched_combine(torch.zeros((2, 4, 8), dtype=torch.bfloat16), idx, w, idx, 0)
