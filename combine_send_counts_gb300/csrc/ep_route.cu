@@ -318,11 +318,13 @@ struct VecOk {
     bool send_idx;     // 16 bytes: pairs of int64
     bool send_w;       // 16 bytes: four floats
     bool is_in_rank;   // 4 bytes: four flags
+    bool token_pos;    // 16 bytes: four ints
 };
 
-static VecOk vec_ok(const int64_t *send_idx, const float *send_w, const uint8_t *is_in_rank)
+static VecOk vec_ok(const int64_t *send_idx, const float *send_w, const uint8_t *is_in_rank,
+                    const int32_t *token_pos = nullptr)
 {
-    return VecOk{aligned(send_idx, 16), aligned(send_w, 16), aligned(is_in_rank, 4)};
+    return VecOk{aligned(send_idx, 16), aligned(send_w, 16), aligned(is_in_rank, 4), aligned(token_pos, 16)};
 }
 
 // Outputs and mode of layout_write_kernel.
@@ -922,11 +924,12 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
     if (a.align > 1)
         fill_pad_rows(s_tot, P, K, a.align, a.num_rows, a.send_token_idx, a.send_rank, a.send_idx, a.send_w);
 
-    if (valid) {
-        int32_t *tp = a.token_pos + t * P;
-        for (int p = 0; p < P; ++p)
-            tp[p] = -1;
-    }
+    // the token's token_pos row is gathered here and written out at the end
+    // with vector stores (one scattered 4-byte store per rank cost the layout
+    // phase most of its store transactions)
+    int32_t tpv[EP_MAX_RANKS];
+    for (int p = 0; p < P; ++p)
+        tpv[p] = -1;
     for (int p = 0; p < P; ++p) {
         const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
         if (!((mask >> p) & 1ull))
@@ -936,7 +939,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
             bad = EP_ERR_CAPACITY;
             continue;
         }
-        a.token_pos[t * P + p] = (int32_t)n;
+        tpv[p] = (int32_t)n;
         a.send_token_idx[n] = (int32_t)t;
         a.send_rank[n] = p;
         const int64_t off = (int64_t)p * El;
@@ -951,6 +954,16 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(FusedArgs a)
                     si[k] = dr[k] == p ? id[k] - off : -1;
                     sw[k] = dr[k] == p ? wt[k] : 0.0f;
                 }
+        }
+    }
+    if (valid) {
+        int32_t *tp = a.token_pos + t * P;
+        if ((P & 3) == 0 && a.vec.token_pos) {
+            for (int p = 0; p < P; p += 4)
+                *reinterpret_cast<int4 *>(tp + p) = make_int4(tpv[p], tpv[p + 1], tpv[p + 2], tpv[p + 3]);
+        } else {
+            for (int p = 0; p < P; ++p)
+                tp[p] = tpv[p];
         }
     }
     raise(a.err, bad);
@@ -1399,7 +1412,7 @@ static int route_nosync(const int64_t *topk_idx, const float *topk_weights, int6
     FusedArgs fa{topk_idx, topk_weights, T, K, P, E_local, num_worst_rows, dest, is_in_rank, send_counts,
                  rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w, token_pos,
                  wl.part_rank, pe, {wl.flags, wl.epoch, next_route_tag()}, align, err,
-                 vec_ok(send_idx, send_w, is_in_rank)};
+                 vec_ok(send_idx, send_w, is_in_rank, token_pos)};
     bool launched = false;
     int rc;
     switch (K) {
