@@ -510,24 +510,34 @@ __global__ void __launch_bounds__(kRouteThreads) layout_write_kernel(LayoutArgs 
         }
         if (valid && dmask != mask)
             bad = EP_ERR_COUNT_MISMATCH;
+        int32_t tpv[EP_MAX_RANKS];   // the token's token_pos row, written out at the end
         for (int p = 0; p < P; ++p) {
             const unsigned bal = __ballot_sync(kFull, (mask >> p) & 1ull);
+            tpv[p] = -1;
             if (!valid)
                 continue;
-            int32_t n = -1;
             if ((mask >> p) & 1ull) {
                 const int64_t pos = (int64_t)s_base[p] + s_warp[warp][p] + __popc(bal & lanemask_lt());
                 if (pos < a.num_rows) {
-                    n = (int32_t)pos;
-                    a.send_token_idx[n] = (int32_t)t;
-                    a.send_rank[n] = p;
+                    tpv[p] = (int32_t)pos;
+                    a.send_token_idx[pos] = (int32_t)t;
+                    a.send_rank[pos] = p;
                     write_send_row<KC>(a.send_idx + pos * KC, a.send_w + pos * KC, id, wt, dr, p,
                                        (int64_t)p * a.E_local, a.vec);
                 } else {
                     bad = a.exact ? EP_ERR_COUNT_MISMATCH : EP_ERR_CAPACITY;
                 }
             }
-            a.token_pos[t * P + p] = n;
+        }
+        if (valid) {
+            int32_t *tp = a.token_pos + t * P;
+            if ((P & 3) == 0 && a.vec.token_pos) {
+                for (int p = 0; p < P; p += 4)
+                    *reinterpret_cast<int4 *>(tp + p) = make_int4(tpv[p], tpv[p + 1], tpv[p + 2], tpv[p + 3]);
+            } else {
+                for (int p = 0; p < P; ++p)
+                    tp[p] = tpv[p];
+            }
         }
         raise(a.err, bad);
         return;
@@ -1369,7 +1379,7 @@ extern "C" int ep_build_send_layout(const int64_t *topk_idx, const float *topk_w
         return EP_ERR_CUDA;
     LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_send, 1, part_rank, nb,
                  nullptr, nullptr, nullptr, nullptr, send_token_idx, send_rank, send_idx, send_w, token_pos, err, 1,
-                 vec_ok(send_idx, send_w, is_in_rank)};
+                 vec_ok(send_idx, send_w, is_in_rank, token_pos)};
     launch_layout_write(a, nb, stream);
     return launch_status();
 }
@@ -1440,7 +1450,7 @@ static int route_nosync(const int64_t *topk_idx, const float *topk_weights, int6
         return EP_ERR_CUDA;
     LayoutArgs a{topk_idx, topk_weights, dest, is_in_rank, T, K, P, E_local, num_worst_rows, 0, wl.part_rank, nb,
                  pe, send_counts, rank_offsets, tokens_per_expert, send_token_idx, send_rank, send_idx, send_w,
-                 token_pos, err, align, vec_ok(send_idx, send_w, is_in_rank)};
+                 token_pos, err, align, vec_ok(send_idx, send_w, is_in_rank, token_pos)};
     launch_layout_write(a, nb, stream);
     return launch_status();
 }
