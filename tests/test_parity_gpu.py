@@ -670,7 +670,7 @@ def test_batched_prepare_many_local_experts():
 
 
 # ----------------------------------- route + dispatch as one no-sync call --
-@pytest.mark.parametrize("name,fp8", [("mid", False), ("large", False), ("chunk_fp8", True)])
+@pytest.mark.parametrize("name,fp8", [("mid", False), ("large", False), ("large", True), ("chunk_fp8", True)])
 def test_dispatch_nosync_matches_oracle(name, fp8):
     w = wl.WORKLOADS[name]
     if name == "chunk_fp8":
