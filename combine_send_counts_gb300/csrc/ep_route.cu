@@ -1484,24 +1484,67 @@ extern "C" int ep_route_nosync_aligned(const int64_t *topk_idx, const float *top
 // passes no workspace.  It exists for callers that cannot allocate device
 // memory themselves: engines that plan all device memory before they start
 // and forbid allocation while they run (for example inside a plugin's enqueue
-// step), and code that must not call cudaMalloc while a CUDA graph is being
-// captured.
+// step, where the host thread must not call into an allocator).
 //
-// The array below is set up once per device: the first call on a device
-// (with that device current) looks up its device address with
-// cudaGetSymbolAddress and caches it.  Every call on a device shares the one
-// array, which keeps the last call's contents; the count kernels overwrite
-// every partial they read, so nothing needs clearing between calls.  Calls
-// whose kernels overlap on the GPU (other streams, other host threads) race
-// on the array.
+// The array below is set up once per device context: the first call on a
+// device (with that device current) looks up its device address with
+// cudaGetSymbolAddress and caches it with the id of the current context; a
+// later call under another context (the device was reset, or its primary
+// context released and created again) looks the address up again instead of
+// reusing a stale one.  Every call on a device shares the one array, which
+// keeps the last call's contents; the count kernels overwrite every partial
+// they read, so nothing needs clearing between calls.  Calls whose kernels
+// overlap on the GPU (other streams, other host threads) race on the array.
+#include <cuda.h>
+
 #include <mutex>
 
 static __device__ __align__(256) unsigned char g_count_scratch[EP_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 constexpr int kMaxDevices = 64;
+
+// The driver API is reached through the runtime's entry-point query, so the
+// library links no libcuda and still loads on a machine without a driver.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+struct ScratchSlot {
+    void *addr = nullptr;
+    unsigned long long ctx_id = 0;
+};
+
 std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
+ScratchSlot g_scratch[kMaxDevices];
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_ctx_fns_looked_up = false;
+
+// Id of the context current on this thread, or 0 if none is current yet or
+// the driver does not offer the query.  Called with g_scratch_mutex held.
+unsigned long long current_context_id()
+{
+    if (!g_ctx_fns_looked_up) {
+        g_ctx_fns_looked_up = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();
+    }
+    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr)
+        return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || g_ctx_get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of g_count_scratch on the current device.  Host code cannot
 // use the symbol itself: on the host it names a stand-in, not device memory.
@@ -1515,15 +1558,49 @@ int count_scratch_address(void **out)
     if (dev < 0 || dev >= kMaxDevices)
         return EP_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchSlot &slot = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    // A cached address is used only under the context it was looked up in;
+    // with no context id to compare (none current yet on this thread), it is
+    // looked up again, which also makes the device's context current.
+    if (slot.addr == nullptr || id == 0 || id != slot.ctx_id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_count_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
+            slot = ScratchSlot{};
             return EP_ERR_CUDA;
         }
-        g_scratch_addr[dev] = p;
+        slot.addr = p;
+        slot.ctx_id = id != 0 ? id : current_context_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
+    return EP_OK;
+}
+
+// The host checks of ep_compute_send_counts that need no workspace, made
+// before the device is touched (looking up the array's address can create
+// the device's context).
+int noalloc_args_status(const int64_t *topk_idx, int64_t T, int K, int P, int E_local,
+                        const int64_t *h_chunk_bounds, int chunks, const int32_t *dest,
+                        const uint8_t *is_in_rank, const int32_t *send_counts)
+{
+    if (!routing_shape_ok(T, K, P, E_local))
+        return EP_ERR_INVALID_ARG;
+    if (chunks > EP_MAX_CHUNKS)
+        return EP_ERR_UNSUPPORTED;
+    if (ep_workspace_size(T, K, P, E_local, chunks) > (size_t)EP_NOALLOC_SCRATCH_BYTES)
+        return EP_ERR_UNSUPPORTED;
+    if (send_counts == nullptr)
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (topk_idx == nullptr || dest == nullptr || is_in_rank == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (chunks > 1) {
+        if (h_chunk_bounds == nullptr || h_chunk_bounds[0] != 0 || h_chunk_bounds[chunks] != T)
+            return EP_ERR_INVALID_ARG;
+        for (int c = 0; c < chunks; ++c)
+            if (h_chunk_bounds[c + 1] < h_chunk_bounds[c])
+                return EP_ERR_INVALID_ARG;
+    }
     return EP_OK;
 }
 }  // namespace
@@ -1533,10 +1610,11 @@ extern "C" int ep_compute_send_counts_noalloc(const int64_t *topk_idx, int64_t T
                                               uint8_t *is_in_rank, int32_t *send_counts, int32_t *rank_offsets,
                                               int32_t *tokens_per_expert, int32_t *err, ep_stream_t stream)
 {
-    if (ep_workspace_size(T, K, P, E_local, chunks) > (size_t)EP_NOALLOC_SCRATCH_BYTES)
-        return EP_ERR_UNSUPPORTED;
+    int rc = noalloc_args_status(topk_idx, T, K, P, E_local, h_chunk_bounds, chunks, dest, is_in_rank, send_counts);
+    if (rc != EP_OK)
+        return rc;
     void *scratch = nullptr;
-    const int rc = count_scratch_address(&scratch);
+    rc = count_scratch_address(&scratch);
     if (rc != EP_OK)
         return rc;
     return ep_compute_send_counts(topk_idx, T, K, P, E_local, h_chunk_bounds, chunks, dest, is_in_rank,

@@ -493,14 +493,17 @@ int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk_probs, int
  * pages have no counterpart of this call; it is for callers that cannot
  * allocate device memory themselves, such as engines that plan all device
  * memory up front and forbid allocation while they run (a plugin's enqueue
- * step), or code that must not call cudaMalloc while a CUDA graph is being
- * captured.
- *   - Sizes whose workspace (ep_workspace_size) exceeds
- *     EP_NOALLOC_SCRATCH_BYTES are rejected with EP_ERR_UNSUPPORTED before
- *     anything is launched (1 MiB covers e.g. T = 65536, P = 16, E = 256).
+ * step, where the host thread must not call into an allocator).
+ *   - Arguments are checked on the host first, as in ep_compute_send_counts
+ *     (EP_ERR_INVALID_ARG), without touching a device.  Sizes whose workspace
+ *     (ep_workspace_size) exceeds EP_NOALLOC_SCRATCH_BYTES are then rejected
+ *     with EP_ERR_UNSUPPORTED before anything is launched (1 MiB covers e.g.
+ *     T = 65536, P = 16, E = 256).
  *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture begins.
+ *     array's device address (cudaGetSymbolAddress) and caches it together
+ *     with the id of the current context; make that first call before any
+ *     stream capture begins.  A call under another context of the device
+ *     (after a device reset, say) looks the address up again.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose kernels
  *     overlap on the GPU -- on other streams or from other host threads --

@@ -148,3 +148,19 @@ def test_helpers_reject_wrong_dtypes_before_any_device_work():
         ep.combine_rows(x32, tp)
     with pytest.raises(TypeError, match="slot must be torch.int32"):
         ep.batched_combine(torch.zeros((2, 4, 8), dtype=torch.bfloat16), idx, w, idx, 0)
+
+
+def test_noalloc_counts_reject_bad_arguments_without_a_device(lib):
+    # The no-allocation counts entry checks its arguments before it looks up
+    # its device array (which would need a device): with no GPU here, a device
+    # call would answer EP_ERR_CUDA instead of these host statuses.
+    f = ep.load().ep_compute_send_counts_noalloc
+    call = lambda T, K, P, El, bounds, C, sc=None: f(None, T, K, P, El, bounds, C, None, None, sc, None, None,
+                                                     None, ctypes.c_void_p(0))
+    assert call(-1, 8, 8, 32, None, 1) == ep.EP_ERR_INVALID_ARG             # T < 0
+    assert call(16, 0, 8, 32, None, 1) == ep.EP_ERR_INVALID_ARG             # K = 0
+    assert call(16, 8, 8, 0, None, 1) == ep.EP_ERR_INVALID_ARG              # E_local = 0
+    assert call(16, 8, 8, 32, None, 1) == ep.EP_ERR_INVALID_ARG             # no send_counts
+    bounds = (ctypes.c_int64 * 3)(0, 4, 15)                                   # does not end at T
+    assert call(16, 8, 8, 32, bounds, 2, ctypes.c_void_p(16)) == ep.EP_ERR_INVALID_ARG
+    assert call(1 << 22, 8, 64, 128, None, 1) == ep.EP_ERR_UNSUPPORTED   # beyond the fixed array
