@@ -301,9 +301,10 @@ def ep_local_expert_fp8(recv_q, recv_scale, send_idx, send_w, N, K, H, out, err,
 
 def ep_compute_send_counts_noalloc(topk_idx, T, K, P, E_local, h_chunk_bounds, chunks, dest, is_in_rank,
                                    send_counts, rank_offsets, tokens_per_expert, err, stream=None):
-    """ep_compute_send_counts without a workspace argument: for callers that
-    cannot allocate device memory, the library's own fixed device array holds
-    the scratch (include/ep.h states its size limit and sharing rules)."""
+    """ep_compute_send_counts without a workspace argument, for callers that
+    cannot allocate device memory: the library's own fixed device array holds
+    the scratch (its size limit and sharing rules are stated beside the C
+    declaration)."""
     hb = None
     if h_chunk_bounds is not None:
         hb = (ctypes.c_int64 * len(h_chunk_bounds))(*[int(v) for v in h_chunk_bounds])
@@ -662,14 +663,16 @@ def local_expert_fp8(recv_q, recv_scale, send_idx, send_w, err=None, stream=None
 
 
 def dispatch_chunked_forward(x, topk_idx, topk_weights, *, num_local_experts: int, num_ranks: int, chunks: int,
-                             fp8: bool = False, local_kernel=None, err=None, stream=None):
+                             fp8: bool = False, local_kernel=None, err=None, stream=None, keep=None):
     """The axolotl dispatch_chunked_forward on one GPU through the native driver.
 
     local_kernel: None for the library's synthetic fp8 expert (fp8 only), or a
     Python callable f(chunk, recv_x, recv_scale, send_idx, send_w, local_out)
     receiving torch views of the chunk's n rows, which must fill local_out
     (bf16 [n, H]) with the weighted sum over K of its experts on the current
-    stream.  Returns out [T,H] bf16."""
+    stream.  keep: an optional dict that receives the driver's buffers (the
+    counts and token_pos of every chunk, and the row buffers, which hold the
+    last chunk's rows once the call has run).  Returns out [T,H] bf16."""
     T, H = x.shape
     K = topk_idx.shape[1]
     P, El = num_ranks, num_local_experts
@@ -720,6 +723,8 @@ def dispatch_chunked_forward(x, topk_idx, topk_weights, *, num_local_experts: in
         cb = LOCAL_KERNEL_FN(_py_kernel)
     ep_dispatch_chunked_forward(x, topk_idx, topk_weights, T, K, H, P, El, chunks, int(fp8), cb, None, out, b,
                                 h_counts, err, stream)
+    if keep is not None:
+        keep.update(t)
     return out
 
 
