@@ -83,3 +83,42 @@ def test_e4m3_special_inputs():
     got = oracle.f32_to_e4m3_bits(f)
     assert got[0] & 0x7F == 0x7F
     assert got[1:].tolist() == [0x7E, 0xFE, 0x7E, 0xFE, 0x7E, 0x7E, 0x80]
+
+
+@pytest.mark.slow
+def test_e4m3_rn_satfinite_exhaustive_over_every_f32_pattern():
+    # Every one of the 2^32 fp32 bit patterns through the oracle's encoder
+    # (OCP OFP8 E4M3, round to nearest even, saturating to +-448; the fp8
+    # payload of NeMo uccl_ep.buffer, Buffer.dispatch), against torch's
+    # conversion of the value clamped to +-448.  NaN inputs must give a NaN
+    # code (exponent and mantissa bits all ones), whatever the sign bit.
+    import concurrent.futures as cf
+    import os
+
+    step = 1 << 24
+    lo, hi = np.float32(-448.0), np.float32(448.0)
+
+    def one(start):
+        bits = np.arange(start, start + step, dtype=np.uint64).astype(np.uint32)
+        f = bits.view(np.float32)
+        ours = oracle.f32_to_e4m3_bits(f)
+        nan = np.isnan(f)
+        with np.errstate(invalid="ignore"):
+            clamped = np.clip(f, lo, hi)
+        ref = torch.from_numpy(clamped).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        ok = np.all(ours[~nan] == ref[~nan]) and np.all((ours[nan] & 0x7F) == 0x7F) \
+            and np.all((ref[nan] & 0x7F) == 0x7F)
+        if ok:
+            return None
+        bad = np.nonzero(np.where(nan, (ours & 0x7F) != 0x7F, ours != ref))[0]
+        i = int(bad[0])
+        return f"pattern {int(bits[i]):#010x}: oracle {int(ours[i]):#04x}, torch {int(ref[i]):#04x}"
+
+    torch_threads = torch.get_num_threads()
+    torch.set_num_threads(1)                       # the pool below is the parallelism
+    try:
+        with cf.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+            errors = [e for e in ex.map(one, range(0, 1 << 32, step)) if e is not None]
+    finally:
+        torch.set_num_threads(torch_threads)
+    assert not errors, errors[:5]
