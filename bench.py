@@ -57,6 +57,12 @@ class L2Flush:
 
 
 # ------------------------------------------------------------ host helpers --
+def workload_name(w) -> str:
+    """The workload as both arms name it in config.workload."""
+    return (f"{w.name}: T={w.T} H={w.H} E={w.E} K={w.K} P={w.P} E_local={w.E_local} "
+            f"routing={w.routing}({w.zipf_s}) weights={w.weights}")
+
+
 def algorithmic_bytes(T: int, H: int, N: int, K: int, P: int) -> dict:
     """Bytes the method must move (each source row read once, each
     destination row written once), per kernel of one step."""
@@ -437,8 +443,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: T={w.T} H={w.H} E={w.E} K={w.K} P={w.P} E_local={w.E_local} "
-                               f"routing={w.routing}({w.zipf_s}) weights={w.weights}",
+        "config": {"workload": workload_name(w),
                    "N_rows": N, "worst_case_rows": sp.W,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps, outside the timed events: a 512 MiB write, then a 256 MiB "
@@ -742,8 +747,9 @@ def cpu_baseline(w, x, idx, wts, y, steps, full=True, T_sample=None):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: each step is the send path on a bounded
-    sample (the first T_sample tokens) of the same workload, on one host core."""
+    """The oracle as the reference arm: each step is the send path on the same
+    workload as the GPU arm (all of its tokens, about half a second per step on
+    one host core), or on its first --reference-tokens tokens if that is set."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -752,7 +758,7 @@ def run_reference(args):
     import oracle
     w = wl.WORKLOADS[args.workload]
     x, idx, wts = wl.make(w)
-    Ts = min(args.reference_tokens, w.T)
+    Ts = w.T if args.reference_tokens <= 0 else min(args.reference_tokens, w.T)
     x, idx, wts = x[:Ts], idx[:Ts], wts[:Ts]
     c = oracle.compute_send_counts(idx, w.P, w.E_local, with_tokens_per_expert=False)
     y = wl.expert_outputs(w, int(c["send_counts"].sum()))
@@ -764,14 +770,17 @@ def run_reference(args):
         oracle_step(oracle, w, x, idx, wts, y)
         times.append(time.perf_counter() - t0)
     tok_s = Ts * len(times) / sum(times)
-    sample = (f"first {Ts} of {w.T} tokens of the {w.name} workload per step; send path (counts, layout, "
-              f"dispatch, combine) in the single-threaded C oracle")
+    which = f"all {w.T} tokens" if Ts == w.T else f"first {Ts} of {w.T} tokens"
+    sample = (f"{which} of the {w.name} workload per step; send path (counts, layout, dispatch, combine) in the "
+              f"single-threaded C oracle")
+    config = {"workload": workload_name(w)}
+    if Ts < w.T:
+        config["T_sample"] = Ts
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: T={w.T} H={w.H} E={w.E} K={w.K} P={w.P} E_local={w.E_local} "
-                               f"routing={w.routing}({w.zipf_s}) weights={w.weights}", "T_sample": Ts},
+        "config": config,
         "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -794,7 +803,8 @@ def main(argv=None):
     ap.add_argument("--e2e-warmup", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=20, help="oracle steps of the CPU baseline (about 0.5 s each on one core)")
-    ap.add_argument("--reference-tokens", type=int, default=4096)
+    ap.add_argument("--reference-tokens", type=int, default=0,
+                    help="reference arm: time the oracle on the first N tokens only (0 = the whole workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
