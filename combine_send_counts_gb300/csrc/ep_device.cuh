@@ -120,12 +120,61 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// ----------------------------------------------- mbarrier + bulk async copy --
+// ------------------------------------------------------ shared-memory addresses --
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------ thread-block clusters --
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: the writes (shared or global) a
+// thread made before it are visible to every thread of the cluster after it.
+// All threads must reach it (no CTA of the cluster may have exited).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Split form of cluster_sync for a barrier phase that orders nothing but
+// the CTAs' start: arrive early, wait later (every CTA of the cluster has
+// started once the wait returns, so its shared memory may be written).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// The 32-bit value at the shared-memory address of *p in CTA `rank` of this
+// cluster (distributed shared memory).
+__device__ __forceinline__ int32_t ld_dsmem_s32(const int32_t *p, uint32_t rank)
+{
+    uint32_t remote;
+    int32_t v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ----------------------------------------------- mbarrier + bulk async copy --
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

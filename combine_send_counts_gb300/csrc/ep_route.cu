@@ -16,6 +16,7 @@
 // is token-ascending by construction.
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "ep_barrier.cuh"
 #include "ep_device.cuh"
@@ -1189,6 +1190,282 @@ static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t 
     return EP_OK;
 }
 
+// ------------------------------------------- expert-batched slots, one cluster --
+// The slots of the expert-batched layout for up to kClMaxCtas * kClTokens
+// tokens, computed by ONE thread-block cluster.  CTA c of the cluster owns the
+// contiguous tokens [c * per_cta, (c + 1) * per_cta) (per_cta <= kClTokens, a
+// multiple of 32), so its ids and slots are the contiguous ranges
+// [c * per_cta * K, ...) of topk_idx and slot:
+//   1. ids are read in position order (consecutive threads, consecutive ids:
+//      coalesced) into a byte table of local experts in shared memory, and
+//      each token's local-expert mask is OR-ed together (by shuffles over its
+//      K lanes when K divides 32, else from its table row);
+//   2. one lane per token (rounds of kClThreads tokens, in token order): the
+//      warp's 32 x 32 bit matrix of masks is transposed by shuffles, so lane e
+//      holds expert e's ballot word (bit l: the warp's token l names e); its
+//      population count is the (round, warp) count;
+//   3. a warp scan turns the counts into bases within the CTA; each CTA writes
+//      its totals into every CTA's shared memory (distributed shared memory,
+//      after a barrier phase begun at the kernel's start shows that every CTA
+//      has started) and one hardware cluster barrier makes them visible: no
+//      flag in global memory is polled and no CTA touches another's memory
+//      after the barrier;
+//   4. slots are written in position order again (coalesced): slot of
+//      position p (token p / K) for expert e = hits of the CTAs before + the
+//      (round, warp) base + the lanes below the token's in e's ballot word.
+// The launch is an ordinary one, so the row scatter after it waits only for
+// this short chain.  Needs E_local <= 64.
+constexpr int kClThreads = 1024;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClRounds = 2;
+constexpr int kClTokens = kClRounds * kClThreads;   // tokens per CTA at most
+constexpr int kClMaxCtas = 16;
+
+struct BatchedClusterArgs {
+    const int64_t *idx;
+    int64_t T;
+    int K, E, E_local;
+    int64_t e0;
+    int per_cta;   // tokens owned by each CTA (the last CTAs may own fewer, or none)
+    SlotLimits lim;
+    int32_t *tokens_per_expert;
+    int32_t *slot;
+    int32_t *err;
+};
+
+// Transpose of the warp's 32 x 32 bit matrix (row l = lane l's word): lane e
+// gets the word whose bit l is bit e of lane l's word.  Recursive block
+// transpose, halving the block size each step (16, 8, 4, 2, 1).
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane)
+{
+    uint32_t m = 0x0000ffffu;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1, m ^= m << j) {
+        const uint32_t y = __shfl_xor_sync(kFull, x, j);
+        x = (lane & j) ? (((y >> j) & m) | (x & ~m)) : ((x & m) | ((y & m) << j));
+    }
+    return x;
+}
+
+// The 32-bit value v into the shared-memory address of *p in CTA `rank` of
+// this cluster.
+__device__ __forceinline__ void st_dsmem_s32(int32_t *p, uint32_t rank, int32_t v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kClThreads, 1) batched_cluster_kernel(BatchedClusterArgs a)
+{
+    allow_dependents();   // the row scatter after this kernel may start loading its input rows
+    cluster_arrive_relaxed();   // waited for before the first write into another CTA's memory
+    // dynamic: [per_cta] local-expert mask of each token, then [per_cta * K]
+    // local expert of each slot (-1 if none)
+    extern __shared__ __align__(16) uint64_t s_dyn[];
+    uint64_t *s_mask = s_dyn;
+    int8_t *s_el = reinterpret_cast<int8_t *>(s_dyn + a.per_cta);
+    // [round][warp][expert] counts, then exclusive bases within the CTA; the
+    // odd row length keeps the scan's column reads free of bank conflicts
+    __shared__ int32_t s_cnt[kClRounds][kClWarps][65];
+    __shared__ uint32_t s_bal[kClRounds][kClWarps][64];   // ballot word per (round, warp, expert)
+    __shared__ int32_t s_tot[kClMaxCtas][64];             // per-expert totals of every CTA
+    const int K = KC > 0 ? KC : a.K;
+    const int El = a.E_local;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t c = cluster_ctarank(), nc = cluster_nctarank();
+    const int64_t t0 = (int64_t)c * a.per_cta;
+    const int64_t left = a.T - t0;
+    const int nloc = left <= 0 ? 0 : (int)(left < a.per_cta ? left : (int64_t)a.per_cta);
+    const int npos = nloc * K;
+    const int64_t *ids = a.idx + t0 * K;
+    constexpr bool kSeg = KC > 0 && 32 % KC == 0;   // a token's K positions share one warp
+    int bad = 0;
+
+    // 1. ids in position order, four loads in flight per thread
+    for (int base = 0; base < npos; base += 4 * kClThreads) {   // uniform over the CTA
+        int64_t v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int p = base + u * kClThreads + threadIdx.x;
+            v[u] = p < npos ? ids[p] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int p = base + u * kClThreads + threadIdx.x;
+            int el = -1;
+            if (p < npos) {
+                if (v[u] < -1 || v[u] >= a.E)
+                    bad = EP_ERR_INVALID_EXPERT;
+                const int64_t d = v[u] - a.e0;
+                el = d >= 0 && d < El ? (int)d : -1;
+                s_el[p] = (int8_t)el;
+            }
+            if constexpr (kSeg) {
+                // OR over the token's KC lanes (p = base + ... + lane, base a
+                // multiple of 32): the lowest of them stores the mask
+                uint64_t m = el >= 0 ? 1ull << el : 0;
+#pragma unroll
+                for (int o = 1; o < KC; o <<= 1)
+                    m |= __shfl_xor_sync(kFull, m, o);
+                if (p < npos && lane % KC == 0)
+                    s_mask[p / KC] = m;
+            }
+        }
+    }
+    __syncthreads();
+    // 2. per (round, warp): transposed masks give each expert's ballot word
+    const int rounds = (nloc + kClThreads - 1) / kClThreads;
+    for (int j = 0; j < rounds; ++j) {   // uniform over the CTA
+        const int tl = j * kClThreads + threadIdx.x;
+        uint64_t mask = 0;
+        if (tl < nloc) {
+            if constexpr (kSeg) {
+                mask = s_mask[tl];
+            } else {
+                for (int k = 0; k < K; ++k) {
+                    const int el = s_el[tl * K + k];
+                    if (el >= 0)
+                        mask |= 1ull << el;
+                }
+            }
+        }
+        const uint32_t w_lo = warp_transpose32((uint32_t)mask, lane);
+        s_bal[j][warp][lane] = w_lo;
+        s_cnt[j][warp][lane] = __popc(w_lo);
+        if (El > 32) {   // uniform
+            const uint32_t w_hi = warp_transpose32((uint32_t)(mask >> 32), lane);
+            s_bal[j][warp][lane + 32] = w_hi;
+            s_cnt[j][warp][lane + 32] = __popc(w_hi);
+        }
+    }
+    __syncthreads();
+    // 3. exclusive scan over (round, warp) of each expert's counts: warp w
+    // scans experts w and w + 32, one lane per warp of the counted round; the
+    // CTA's total goes to every CTA of the cluster, all of which have started
+    // once the wait returns
+    cluster_wait();
+    for (int e = warp; e < El; e += kClWarps) {
+        int run = 0;
+        for (int j = 0; j < rounds; ++j) {
+            const int v = s_cnt[j][lane][e];
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o)
+                    incl += n;
+            }
+            s_cnt[j][lane][e] = run + incl - v;
+            run += __shfl_sync(kFull, incl, 31);
+        }
+        if (lane < (int)nc)
+            st_dsmem_s32(&s_tot[c][e], (uint32_t)lane, run);
+    }
+    // every CTA's totals are in every CTA's s_tot, and the bases are visible
+    // to the whole CTA; after this barrier no CTA touches another's memory
+    cluster_sync();
+    __shared__ int32_t s_pre[64];   // hits of the CTAs before this one
+    if (threadIdx.x < El) {
+        const int e = threadIdx.x;
+        int pre = 0, tot = 0;
+        for (int cc = 0; cc < (int)nc; ++cc) {
+            const int v = s_tot[cc][e];
+            pre += cc < (int)c ? v : 0;
+            tot += v;
+        }
+        s_pre[e] = pre;
+        if (c == 0)
+            bad |= finish_expert_count(a.lim, e, tot, a.tokens_per_expert);
+    }
+    __syncthreads();
+    // 4. slots in position order
+    int32_t *out = a.slot + t0 * K;
+    for (int p = threadIdx.x; p < npos; p += kClThreads) {
+        const int el = s_el[p];
+        int32_t sl = -1;
+        if (el >= 0) {
+            const int tl = p / K;
+            const int j = tl / kClThreads, w = (tl / 32) % kClWarps, l = tl % 32;
+            const int s = s_pre[el] + s_cnt[j][w][el] + __popc(s_bal[j][w][el] & ((1u << l) - 1u));
+            sl = s < a.lim.cap ? s : -1;
+            if (s >= a.lim.cap && !a.lim.silent)
+                bad = EP_ERR_CAPACITY;
+        }
+        out[p] = sl;
+    }
+    raise(a.err, bad);
+}
+
+// Cluster size for the one-cluster slot kernel: 16 CTAs where the device
+// schedules such clusters (a non-portable size), else 8; 0 if neither.
+template <int KC>
+static int batched_cluster_size()
+{
+    static std::atomic<int> size{-1};
+    int n = size.load(std::memory_order_relaxed);
+    if (n >= 0)
+        return n;
+    n = 0;
+    if (cudaFuncSetAttribute(batched_cluster_kernel<KC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(batched_cluster_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kClTokens * (8 + EP_MAX_TOPK)) != cudaSuccess)
+        cudaGetLastError();
+    for (int cs : {16, 8}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs);
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = kClTokens * (8 + EP_MAX_TOPK);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, batched_cluster_kernel<KC>, &cfg) == cudaSuccess &&
+            clusters >= 1) {
+            n = cs;
+            break;
+        }
+        cudaGetLastError();
+    }
+    size.store(n, std::memory_order_relaxed);
+    return n;
+}
+
+template <int KC>
+static int launch_batched_cluster(const BatchedClusterArgs &a0, cudaStream_t stream, bool *launched)
+{
+    *launched = false;
+    const int cs = batched_cluster_size<KC>();
+    if (cs == 0 || a0.T > (int64_t)cs * kClTokens)
+        return EP_OK;   // the caller takes the grid-wide form
+    BatchedClusterArgs a = a0;
+    a.per_cta = (int)align_up((size_t)ceil_div(a.T, cs), 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = (size_t)a.per_cta * (8 + a.K);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, batched_cluster_kernel<KC>, a) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    *launched = true;
+    return EP_OK;
+}
+
 int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E_local, int rank,
                          const SlotLimits &lim, int32_t *tokens_per_expert, int32_t *slot,
                          void *ws, size_t ws_bytes, int32_t *err, cudaStream_t stream, const RowPrefetch &pf)
@@ -1200,8 +1477,24 @@ int launch_batched_slots(const int64_t *topk_idx, int64_t T, int K, int E, int E
                 return EP_ERR_CUDA;
         return EP_OK;
     }
-    // one cooperative launch when the local experts fit one mask word, the
-    // blocks can be resident together and the workspace holds partials + flags
+    // one cluster when the local experts fit one mask word and the tokens fit
+    // the cluster's rounds
+    if (E_local <= 64) {
+        BatchedClusterArgs ca{topk_idx, T, K, E, E_local, e0, 0, lim, tokens_per_expert, slot, err};
+        bool launched = false;
+        int rc;
+        switch (K) {
+        case 2: rc = launch_batched_cluster<2>(ca, stream, &launched); break;
+        case 4: rc = launch_batched_cluster<4>(ca, stream, &launched); break;
+        case 6: rc = launch_batched_cluster<6>(ca, stream, &launched); break;
+        case 8: rc = launch_batched_cluster<8>(ca, stream, &launched); break;
+        default: rc = launch_batched_cluster<0>(ca, stream, &launched); break;
+        }
+        if (rc != EP_OK || launched)
+            return rc;
+    }
+    // else one cooperative launch when the blocks can be resident together and
+    // the workspace holds partials + flags
     // workspace: [header: launch counter][partials][flags]
     char *wsb = static_cast<char *>(ws);
     const int nbf = (int)ceil_div(T, kFusedThreads);
