@@ -23,6 +23,7 @@
 #include <cuda_fp16.h>
 
 #include "ep_device.cuh"
+#include "ep_fp8.cuh"
 #include "ep_internal.h"
 #include "ep_rows.cuh"
 
@@ -121,88 +122,13 @@ scatter_bf16_kernel(const uint4 *__restrict__ x, int64_t T, Geometry g, Rows row
 }
 
 // ------------------------------------------------- fp8 (1x128) scatter --
-// Where and how the group scales go: the layout (EP_SCALE_*) and whether the
-// scales are powers of two.  Column-major layouts index destination row
-// r = e * M + s as (e, s).
-struct ScaleSpec {
-    void *out;
-    int fmt;
-    int round;
-    int M;
-};
-
-// Index of group 0's scale of destination row r (4-byte entries; bytes for
-// UE8M0), computed once per row; put_scale adds the group's offset.
-template <int SF>
-__device__ __forceinline__ int64_t scale_row_base(const ScaleSpec &sp, int32_t r, int groups)
-{
-    if (SF == EP_SCALE_ROW_F32)
-        return (int64_t)r * groups;
-    const int e = r / sp.M, s = r - e * sp.M;
-    if (SF == EP_SCALE_COL_F32)
-        return (int64_t)e * groups * sp.M + s;
-    return ((int64_t)e * (groups >> 2) * sp.M + s) * 4;
-}
-
-template <int SF>
-__device__ __forceinline__ void put_scale(const ScaleSpec &sp, int64_t base, int gi, float sc, uint32_t code)
-{
-    if (SF == EP_SCALE_ROW_F32)
-        static_cast<float *>(sp.out)[base + gi] = sc;
-    else if (SF == EP_SCALE_COL_F32)
-        static_cast<float *>(sp.out)[base + (int64_t)gi * sp.M] = sc;
-    else
-        static_cast<uint8_t *>(sp.out)[base + (int64_t)(gi >> 2) * sp.M * 4 + (gi & 3)] = (uint8_t)code;
-}
-
-// Group maxima of one chunk.  m[u] is a lane's own maximum over the 8 values
-// of its vector u; a group is vector u of the 16 lanes of one half-warp.  The
-// first log2(U) butterfly steps each hand half of a lane's values to its
-// partner, so that lane l ends with the whole maximum of group
-// u = (l >> 2) & 3 (U = 4) or (l >> 3) & 1 (U = 2) of its half-warp after
-// U + 3 shuffles (instead of 4U).  max is exact, so the order of the steps
-// does not change the value.
-template <int U>
-__device__ __forceinline__ float half_warp_group_max(const float (&m)[U], int lane)
-{
-    static_assert(U == 2 || U == 4, "two or four vectors per lane");
-    float k;
-    if constexpr (U == 4) {
-        const bool b3 = lane & 8, b2 = lane & 4;
-        const float k0 = fmaxf(b3 ? m[2] : m[0], __shfl_xor_sync(kFull, b3 ? m[0] : m[2], 8));
-        const float k1 = fmaxf(b3 ? m[3] : m[1], __shfl_xor_sync(kFull, b3 ? m[1] : m[3], 8));
-        k = fmaxf(b2 ? k1 : k0, __shfl_xor_sync(kFull, b2 ? k0 : k1, 4));
-    } else {
-        const bool b3 = lane & 8;
-        k = fmaxf(b3 ? m[1] : m[0], __shfl_xor_sync(kFull, b3 ? m[0] : m[1], 8));
-        k = fmaxf(k, __shfl_xor_sync(kFull, k, 4));
-    }
-    k = fmaxf(k, __shfl_xor_sync(kFull, k, 2));
-    return fmaxf(k, __shfl_xor_sync(kFull, k, 1));
-}
-
-// the vector u whose group maximum lane l holds after half_warp_group_max
-template <int U>
-__device__ __forceinline__ int group_owner_u(int lane)
-{
-    return U == 4 ? (lane >> 2) & 3 : (lane >> 3) & 1;
-}
-
-// fp8 (1x128) scatter, one warp per token (grid-stride loop over tokens).
-// Lanes j < D (and j + 32) resolve the token's rows; the warp quantises the
-// row once, in chunks of U 16-byte vectors per lane, where lanes 0-15 and
-// 16-31 each hold one 128-element group (group max by half-warp shuffles), and
-// writes each chunk's e4m3 codes and group scales to every row, taking the
-// rows by shuffle.  The 2U group maxima of a chunk end up one per lane
-// quad (or octet), so each group's scale is divided out once, by the lane
-// that then stores it, and its reciprocal is handed to the group's lanes by
+// One warp per token (grid-stride loop over tokens).  Lanes j < D (and
+// j + 32) resolve the token's rows; the warp quantises the row once, in
+// chunks of U 16-byte vectors per lane (quantize_chunk), and writes each
+// chunk's e4m3 codes and group scales to every row, taking the rows by
 // shuffle; a destination row's scale base is computed once per token.  No
-// shared memory and no block barrier.  With a = max(max|x|, 1e-4):
-//   plain (RS = false): q = e4m3_rn_satfinite(x * (448 / a)), scale = a / 448;
-//   power of two:       scale = 2^e, the smallest power of two >= a / 448 (from
-//                       the bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
-//                       UE8M0 code e + 127.
-// SF is the scale layout (EP_SCALE_*).
+// shared memory and no block barrier.  SF is the scale layout (EP_SCALE_*),
+// RS selects power-of-two scales.
 template <int U, class Rows, int SF, bool RS, bool DB>
 __global__ void __launch_bounds__(kMoveThreads, DB ? 3 : 4)
 scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows rows, int64_t n_rows,
@@ -272,43 +198,10 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
                         vin[u] = ld_stream(src + i);
                 }
             }
-            float m[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {   // vectors past the row are whole half-warps of zeros
-                const uint32_t w[4] = {vin[u].x, vin[u].y, vin[u].z, vin[u].w};
-                m[u] = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    m[u] = fmaxf(m[u], fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
-            }
-            // this lane's group: its scale (and UE8M0 code) and the reciprocal
-            const float a = fmaxf(half_warp_group_max<U>(m, lane), 1e-4f);
-            float inv_own, scale_own;
-            uint32_t code_own = 0;
-            if (RS) {
-                const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
-                const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
-                scale_own = __uint_as_float(eb << 23);
-                inv_own = __uint_as_float((254u - eb) << 23);
-                code_own = eb;
-            } else {
-                inv_own = __fdiv_rn(448.0f, a);
-                scale_own = __fdiv_rn(a, 448.0f);
-            }
             uint2 q[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const float inv = __shfl_sync(kFull, inv_own, (lane & 16) | (U == 4 ? u << 2 : u << 3));
-                const float2 inv2 = make_float2(inv, inv);
-                const uint32_t w[4] = {vin[u].x, vin[u].y, vin[u].z, vin[u].w};
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 pr = mul2_rn(make_float2(bf16_lo(w[e]), bf16_hi(w[e])), inv2);
-                    packed[e] = (uint32_t)__nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
-                }
-                q[u] = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
-            }
+            float scale_own;
+            uint32_t code_own;
+            quantize_chunk<U, RS>(vin, lane, q, scale_own, code_own);
             const bool put = owner && base + i_own < nvec;
             for (uint64_t mm = valid; mm != 0; mm &= mm - 1) {   // warp-uniform
                 const int j = __ffsll((long long)mm) - 1;
@@ -328,6 +221,89 @@ scatter_fp8_warp_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, Rows r
                 if (put)
                     put_scale<SF>(sp, sb, (base + i_own) >> 4, scale_own, code_own);
             }
+        }
+    }
+    raise(err, bad);
+}
+
+// fp8 (1x128) scatter on the expert-batched layout, in balanced units.  A
+// unit is one chunk (32 * U 16-byte vectors) of one token's row; warp w of
+// the grid owns the contiguous units [w * units / nw, (w + 1) * units / nw),
+// so every warp quantises the same number of chunks and the grid is one
+// resident wave (no partial last wave of blocks: the per-token form, one
+// token per warp in 1024 blocks of which 608 are resident, left the SMs idle
+// for a quarter of its time).  A warp takes its units in order, resolving a
+// token's rows (lanes j < K) once per token.
+template <int U, int SF, bool RS>
+__global__ void __launch_bounds__(kMoveThreads, 4)
+scatter_fp8_units_kernel(const uint4 *__restrict__ x, int64_t T, int nvec, BatchedRows rows, int64_t n_rows,
+                         int err_bits, uint2 *__restrict__ out_q, ScaleSpec sp, int32_t *err)
+{
+    const int lane = threadIdx.x & 31;
+    constexpr int kChunk = 32 * U;   // vectors per unit
+    const int nch = (nvec + kChunk - 1) / kChunk;
+    const int64_t units = T * nch;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t u_lo = gw * units / nw, u_hi = (gw + 1) * units / nw;
+    grid_dependency_wait();
+    allow_dependents();   // a zero fill after this kernel reads only what the kernel before it wrote
+    const int groups = nvec / 16;
+    const int u_own = group_owner_u<U>(lane);
+    const int i_own = 32 * u_own + (lane & 16);
+    const bool owner = (lane & (U == 4 ? 3 : 7)) == 0;
+    int bad = 0;
+    int64_t cur = -1;
+    int32_t r = -1;       // lane j < K: the token's row for slot j, or -1
+    int64_t sbase = 0;    // its scale base (column layouts)
+    unsigned valid = 0;
+    for (int64_t u = u_lo; u < u_hi; ++u) {
+        const int64_t t = u / nch;
+        if (t != cur) {
+            cur = t;
+            r = -1;
+            sbase = 0;
+            if (lane < rows.len()) {
+                r = rows.row(t, lane);
+                if (r >= n_rows) {
+                    bad = err_bits;
+                    r = -1;
+                }
+                if (SF != EP_SCALE_ROW_F32 && r >= 0)
+                    sbase = scale_row_base<SF>(sp, r, groups);
+            }
+            valid = __ballot_sync(kFull, r >= 0);
+        }
+        if (valid == 0)
+            continue;   // warp-uniform: a token with no row here is not read
+        const int base = (int)(u - t * nch) * kChunk;
+        const uint4 *src = x + t * nvec;
+        uint4 vin[U];
+#pragma unroll
+        for (int u2 = 0; u2 < U; ++u2) {   // all loads first: U vectors in flight
+            const int i = base + lane + 32 * u2;
+            vin[u2] = make_uint4(0, 0, 0, 0);
+            if (i < nvec)
+                vin[u2] = ld_stream(src + i);
+        }
+        uint2 q[U];
+        float scale_own;
+        uint32_t code_own;
+        quantize_chunk<U, RS>(vin, lane, q, scale_own, code_own);
+        const bool put = owner && base + i_own < nvec;
+        for (unsigned mm = valid; mm != 0; mm &= mm - 1) {   // warp-uniform
+            const int j = __ffs(mm) - 1;
+            const int32_t rj = __shfl_sync(kFull, r, j);
+            const int64_t sb = SF == EP_SCALE_ROW_F32 ? (int64_t)rj * groups : __shfl_sync(kFull, sbase, j);
+            uint2 *dq = out_q + (int64_t)rj * nvec;
+#pragma unroll
+            for (int u2 = 0; u2 < U; ++u2) {
+                const int i = base + lane + 32 * u2;
+                if (i < nvec)
+                    st_stream(dq + i, q[u2]);
+            }
+            if (put)
+                put_scale<SF>(sp, sb, (base + i_own) >> 4, scale_own, code_own);
         }
     }
     raise(err, bad);
@@ -607,23 +583,58 @@ static int launch_scatter_fp8(const void *x, int64_t T, int H, const SendRows &r
                                                                      err, stream, dependent);
 }
 
+template <int SF, bool RS>
+static int launch_scatter_fp8_units(const void *x, int64_t T, int H, const BatchedRows &rows, int64_t n_rows,
+                                    int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream,
+                                    bool dependent)
+{
+    const int nvec = H / 8;
+    const bool u4 = nvec > 64;
+    auto kernel = u4 ? scatter_fp8_units_kernel<4, SF, RS> : scatter_fp8_units_kernel<2, SF, RS>;
+    static std::atomic<int> per_sm_cache[2] = {{-1}, {-1}};
+    int per_sm = per_sm_cache[u4].load(std::memory_order_relaxed);
+    if (per_sm < 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kMoveThreads, 0) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        per_sm = std::max(n, 1);
+        per_sm_cache[u4].store(per_sm, std::memory_order_relaxed);
+    }
+    const int chunk = 32 * (u4 ? 4 : 2);
+    const int64_t units = T * ((nvec + chunk - 1) / chunk);
+    // one resident wave, but at least about four units per warp
+    const int64_t blocks = std::min<int64_t>((int64_t)per_sm * device_sm_count(),
+                                             std::max<int64_t>(1, ceil_div(units, 4 * (kMoveThreads / 32))));
+    if (T == 0)
+        return EP_OK;
+    const cudaError_t e = launch_kernel(dependent, kernel, dim3((unsigned)blocks), dim3(kMoveThreads), 0, stream,
+                                        static_cast<const uint4 *>(x), T, nvec, rows, n_rows, err_bits,
+                                        static_cast<uint2 *>(out_q), sp, err);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
 static int launch_scatter_fp8(const void *x, int64_t T, int H, const BatchedRows &rows, int64_t n_rows,
                               int err_bits, void *out_q, const ScaleSpec &sp, int32_t *err, cudaStream_t stream,
                               bool dependent)
 {
     if (sp.fmt == EP_SCALE_COL_UE8M0)
-        return launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_UE8M0, true>(x, T, H, rows, n_rows, err_bits,
-                                                                            out_q, sp, err, stream, dependent);
+        return launch_scatter_fp8_units<EP_SCALE_COL_UE8M0, true>(x, T, H, rows, n_rows, err_bits, out_q, sp, err,
+                                                                  stream, dependent);
     if (sp.fmt == EP_SCALE_COL_F32)
-        return sp.round ? launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_F32, true>(x, T, H, rows, n_rows, err_bits,
-                                                                                     out_q, sp, err, stream, dependent)
-                        : launch_scatter_fp8_as<BatchedRows, EP_SCALE_COL_F32, false>(x, T, H, rows, n_rows,
-                                                                                      err_bits, out_q, sp, err,
-                                                                                      stream, dependent);
-    return sp.round ? launch_scatter_fp8_as<BatchedRows, EP_SCALE_ROW_F32, true>(x, T, H, rows, n_rows, err_bits,
-                                                                                 out_q, sp, err, stream, dependent)
-                    : launch_scatter_fp8_as<BatchedRows, EP_SCALE_ROW_F32, false>(x, T, H, rows, n_rows, err_bits,
-                                                                                  out_q, sp, err, stream, dependent);
+        return sp.round ? launch_scatter_fp8_units<EP_SCALE_COL_F32, true>(x, T, H, rows, n_rows, err_bits, out_q,
+                                                                           sp, err, stream, dependent)
+                        : launch_scatter_fp8_units<EP_SCALE_COL_F32, false>(x, T, H, rows, n_rows, err_bits, out_q,
+                                                                            sp, err, stream, dependent);
+    return sp.round ? launch_scatter_fp8_units<EP_SCALE_ROW_F32, true>(x, T, H, rows, n_rows, err_bits, out_q, sp,
+                                                                       err, stream, dependent)
+                    : launch_scatter_fp8_units<EP_SCALE_ROW_F32, false>(x, T, H, rows, n_rows, err_bits, out_q, sp,
+                                                                        err, stream, dependent);
 }
 
 static bool row_shape_ok(int64_t T, int H)
@@ -718,14 +729,14 @@ static int batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, in
     int32_t *kept = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + slot_ws);
 
     const SlotLimits lim{M, capacity > 0 ? capacity : M, capacity > 0, alignment, dropped, kept};
-    // the slot kernel brings the rows the bf16 scatter reads into the L2 (up
-    // to three quarters of it) while its blocks wait for one another; the fp8
-    // scatter is bound by its arithmetic, not its reads, and gains nothing
+    // the slot kernel, then the row scatter as its dependent; where the slot
+    // kernel has a grid-wide wait, its blocks ask the L2 for the rows the
+    // bf16 scatter reads (up to three quarters of it) while they wait
     const int64_t row_bytes = (int64_t)H * 2;
     const RowPrefetch pf{sp == nullptr ? x : nullptr, row_bytes,
                          std::min<int64_t>(T, device_l2_bytes() / 4 * 3 / row_bytes)};
-    int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, lim, tokens_per_expert, slot, ws, slot_ws,
-                                  err, stream, pf);
+    int rc = launch_batched_slots(topk_idx, T, K, E, E_local, rank, lim, tokens_per_expert, slot, ws, slot_ws, err,
+                                  stream, pf);
     if (rc != EP_OK)
         return rc;
     if (T > 0) {

@@ -21,6 +21,7 @@
 #include "ep_barrier.cuh"
 #include "ep_device.cuh"
 #include "ep_internal.h"
+#include "ep_slots.cuh"
 
 namespace ep {
 
@@ -283,33 +284,6 @@ __device__ __forceinline__ void fill_pad_rows(const int32_t *pad_first, int P, i
             }
         }
     }
-}
-
-__device__ __forceinline__ void block_rank_sums(const int32_t *__restrict__ part, int nb, int P, int b,
-                                                int32_t *s_tot, int32_t *s_before)
-{
-    const int nsl = blockDim.x / P;
-    const int p = threadIdx.x % P, sl = threadIdx.x / P;
-    if (sl >= nsl)
-        return;
-    int tot = 0, bef = 0;
-    for (int bb0 = sl; bb0 < nb; bb0 += nsl * 8) {
-        int v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int bb = bb0 + u * nsl;
-            v[u] = bb < nb ? part[(int64_t)bb * P + p] : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            tot += v[u];
-            bef += (bb0 + u * nsl < b) ? v[u] : 0;
-        }
-    }
-    if (tot != 0)
-        atomicAdd(&s_tot[p], tot);
-    if (bef != 0)
-        atomicAdd(&s_before[p], bef);
 }
 
 // Which layout outputs are aligned for vector stores: the C ABI promises
@@ -653,18 +627,6 @@ batched_count_kernel(const int64_t *__restrict__ idx, int64_t T, int K, int E, i
         __syncthreads();
     }
     raise(err, bad);
-}
-
-// Block 0's per-expert totals: kept count, aligned tokens_per_expert, drops.
-__device__ __forceinline__ int finish_expert_count(const SlotLimits &L, int e, int tot, int32_t *tokens_per_expert)
-{
-    const int kept = min(tot, L.cap);
-    tokens_per_expert[e] = min((kept + L.align - 1) / L.align * L.align, L.M);
-    if (L.dropped != nullptr)
-        L.dropped[e] = tot - kept;
-    if (L.kept != nullptr)
-        L.kept[e] = kept;
-    return tot > L.cap && !L.silent ? EP_ERR_CAPACITY : 0;
 }
 
 __global__ void __launch_bounds__(kRouteThreads)
@@ -1232,20 +1194,6 @@ struct BatchedClusterArgs {
     int32_t *slot;
     int32_t *err;
 };
-
-// Transpose of the warp's 32 x 32 bit matrix (row l = lane l's word): lane e
-// gets the word whose bit l is bit e of lane l's word.  Recursive block
-// transpose, halving the block size each step (16, 8, 4, 2, 1).
-__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane)
-{
-    uint32_t m = 0x0000ffffu;
-#pragma unroll
-    for (int j = 16; j > 0; j >>= 1, m ^= m << j) {
-        const uint32_t y = __shfl_xor_sync(kFull, x, j);
-        x = (lane & j) ? (((y >> j) & m) | (x & ~m)) : ((x & m) | ((y & m) << j));
-    }
-    return x;
-}
 
 // The 32-bit value v into the shared-memory address of *p in CTA `rank` of
 // this cluster.

@@ -124,3 +124,43 @@ def test_batched_fp8_empty_and_host_checks():
     with pytest.raises(ep.EPError):
         ep.batched_prepare_fp8(torch.zeros((4, 512), dtype=torch.bfloat16, device=dev), idx, 4, 4, 0, 8,
                                ep.EP_SCALE_COL_UE8M0, False)                                 # no round_scale
+
+
+def _min_workspace(T, El):
+    """The smallest workspace the batched prepare accepts: a header, one count
+    per (256-token block, local expert) and the kept counts.  Too small for the
+    cooperative slot kernel's flags, so larger problems take the count and
+    slot kernels."""
+    kept = -(-El * 4 // 256) * 256
+    return torch.zeros(256 + (-(-T // 256)) * El * 4 + kept, dtype=torch.uint8, device="cuda")
+
+
+# T, H, K, E, E_local, rank, M, workspace: every slot kernel in front of the
+# fp8 row scatter
+SLOT_FORMS = [
+    (3000, 256, 6, 192, 96, 1, 1000, "full"),      # more than 64 local experts: count + slot kernels
+    (3000, 256, 8, 64, 32, 1, 1000, "min"),        # one cluster (needs no workspace)
+    (50000, 128, 8, 64, 32, 1, 8000, "min"),       # past the cluster's size, no room for flags: count + slot kernels
+    (160000, 128, 8, 64, 32, 1, 22000, "full"),    # past the cluster's size: the cooperative slot kernel
+]
+
+
+@pytest.mark.parametrize("T,H,K,E,El,rank,M,wsk", SLOT_FORMS)
+def test_batched_fp8_every_slot_kernel_matches_oracle(T, H, K, E, El, rank, M, wsk):
+    fmt, rs = ep.EP_SCALE_COL_F32, 0
+    idx, _ = routing_inputs(T, K, E, T + 7, 0.1)
+    x = _wide_rows(T, H, T + 8)
+    dev = "cuda"
+    b_q = torch.empty((El, M, H), dtype=torch.uint8, device=dev)
+    shape, dt = ep.batched_scale_storage(El, M, H, fmt)
+    b_s = torch.empty(shape, dtype=dt, device=dev)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws = ep.workspace(T, K, E // El, El) if wsk == "full" else _min_workspace(T, El)
+    err = ep.error_word()
+    ep.ep_batched_prepare_fp8(x.cuda(), idx.cuda(), T, K, H, E, El, rank, M, b_q, b_s, fmt, rs, tpe, slot, 0, ws,
+                              err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, ep.ep_status_str(int(err.item()))
+    o = oracle.batched_prepare_fp8(x, idx, E, El, rank, M, fmt, False)
+    _compare(dict(tokens_per_expert=tpe, slot=slot, b_q=b_q, b_scale=b_s), o, fmt, check_all=False)

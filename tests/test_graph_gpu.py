@@ -141,3 +141,44 @@ def test_batched_prepare_combine_graph_replays_new_routing(T, H, K, E, El, rank,
         assert_equal(f"b_x/{seed}", bits16(b_x), o["b_x"])
         o_out = oracle.batched_combine(o["b_x"], hi, hw, o["slot"], El, rank)
         assert_combine_parity(f"batched combine/{seed}", bits16(out), o_out)
+
+
+@pytest.mark.parametrize("fmt,rs", [(ep.EP_SCALE_COL_F32, 0), (ep.EP_SCALE_COL_UE8M0, 1)])
+@pytest.mark.parametrize("T,H,K,E,El,rank,M", [(6000, 512, 8, 64, 16, 2, 3000), (999, 512, 4, 32, 32, 0, 700)])
+def test_batched_prepare_fp8_graph_replays_new_routing(T, H, K, E, El, rank, M, fmt, rs):
+    # slot kernel + fp8 row scatter (its programmatic dependent) + zero fill,
+    # replayed on new routing: every output is recomputed by each replay
+    dev = "cuda"
+    idx = torch.empty((T, K), dtype=torch.int64, device=dev)
+    x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    shape, dt = ep.batched_scale_storage(El, M, H, fmt)
+    b_q = torch.empty((El, M, H), dtype=torch.uint8, device=dev)
+    b_s = torch.empty(shape, dtype=dt, device=dev)
+    tpe = torch.empty(El, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws = ep.workspace(T, K, E // El, El, 1)
+    err = ep.error_word()
+
+    def step():
+        s = torch.cuda.current_stream()
+        ep.ep_batched_prepare_fp8(x, idx, T, K, H, E, El, rank, M, b_q, b_s, fmt, rs, tpe, slot, 1, ws, err, s)
+
+    i0, _ = routing_inputs(T, K, E, 71, 0.1)
+    idx.copy_(i0)
+    x.copy_(randn_bf16(T, H, 72))
+    g = _capture(step, torch.cuda.Stream())
+    for seed, fu in REPLAYS:
+        hi, _ = routing_inputs(T, K, E, seed, fu)
+        hx = randn_bf16(T, H, seed + 3)
+        idx.copy_(hi)
+        x.copy_(hx)
+        err.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, ep.ep_status_str(int(err.item()))
+        o = oracle.batched_prepare_fp8(hx, hi, E, El, rank, M, fmt, bool(rs), zero_pad=True)
+        assert_equal(f"tokens_per_expert/{seed}", np_(tpe), o["tokens_per_expert"])
+        assert_equal(f"slot/{seed}", np_(slot), o["slot"])
+        assert_equal(f"codes/{seed}", np_(b_q), o["b_q"])
+        assert_equal(f"scales/{seed}", np_(b_s).view(np.uint32), o["b_scale"].view(np.uint32))
