@@ -1228,7 +1228,7 @@ __global__ void __launch_bounds__(kClThreads, 1) batched_cluster_kernel(BatchedC
     const int nloc = left <= 0 ? 0 : (int)(left < a.per_cta ? left : (int64_t)a.per_cta);
     const int npos = nloc * K;
     const int64_t *ids = a.idx + t0 * K;
-    constexpr bool kSeg = KC > 0 && 32 % KC == 0;   // a token's K positions share one warp
+    constexpr bool kSeg = KC > 0 && 32 % (KC > 0 ? KC : 1) == 0;   // a token's K positions share one warp
     int bad = 0;
 
     // 1. ids in position order, four loads in flight per thread
