@@ -103,7 +103,7 @@ def measured_peak() -> tuple:
 KERNEL_SOURCES = {
     "dispatch": ["ep_move.cu", "ep_rows.cuh", "ep_device.cuh", "ep_internal.h"],
     "combine": ["ep_combine.cu", "ep_rows.cuh", "ep_device.cuh", "ep_internal.h"],
-    "route": ["ep_route.cu", "ep_barrier.cuh", "ep_device.cuh", "ep_internal.h"],
+    "route": ["ep_route.cu", "ep_barrier.cuh", "ep_slots.cuh", "ep_device.cuh", "ep_internal.h"],
 }
 
 
