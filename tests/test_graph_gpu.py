@@ -31,9 +31,10 @@ def _capture(fn, stream):
     return g
 
 
+@pytest.mark.parametrize("with_tpe", [True, False])
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("T,H,K,P,El", [(5000, 256, 8, 8, 4), (1537, 136, 6, 16, 2)])
-def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El, fused):
+def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El, fused, with_tpe):
     dev = "cuda"
     W = T * min(K, P)
     idx = torch.empty((T, K), dtype=torch.int64, device=dev)
@@ -43,7 +44,7 @@ def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El, fused)
     o_iir = torch.empty((T, P), dtype=torch.uint8, device=dev)
     o_sc = torch.empty(P, dtype=torch.int32, device=dev)
     o_ro = torch.empty(P + 1, dtype=torch.int32, device=dev)
-    o_tpe = torch.empty(P * El, dtype=torch.int32, device=dev)
+    o_tpe = torch.empty(P * El, dtype=torch.int32, device=dev) if with_tpe else None
     o_sti = torch.empty(W, dtype=torch.int32, device=dev)
     o_sr = torch.empty(W, dtype=torch.int32, device=dev)
     o_si = torch.empty((W, K), dtype=torch.int64, device=dev)
@@ -89,7 +90,8 @@ def test_route_dispatch_combine_graph_replays_new_routing(T, H, K, P, El, fused)
         assert_equal(f"dest/{seed}", np_(o_dest), oc["dest"])
         assert_equal(f"is_in_rank/{seed}", np_(o_iir), oc["is_in_rank"])
         assert_equal(f"send_counts/{seed}", np_(o_sc), oc["send_counts"])
-        assert_equal(f"tokens_per_expert/{seed}", np_(o_tpe), oc["tokens_per_expert"])
+        if with_tpe:
+            assert_equal(f"tokens_per_expert/{seed}", np_(o_tpe), oc["tokens_per_expert"])
         assert int(o_ro[P].item()) == N
         for k, t in (("send_token_idx", o_sti), ("send_rank", o_sr), ("send_idx", o_si)):
             assert_equal(f"{k}/{seed}", np_(t)[:N], ol[k])

@@ -315,8 +315,10 @@ def test_batched_duplicate_experts_small():
 
 
 # --------------------------------------------------- no-sync (worst-case) path --
+# with_tpe: tokens_per_expert asked for, or not (no expert partials)
+@pytest.mark.parametrize("with_tpe", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "mid", "large"])
-def test_route_nosync_matches_oracle(name):
+def test_route_nosync_matches_oracle(name, with_tpe):
     w = wl.WORKLOADS[name]
     x, idx, wts = wl.make(w)
     o = oracle.send_path(x, idx, wts, None, w.P, w.E_local)
@@ -324,7 +326,7 @@ def test_route_nosync_matches_oracle(name):
     y = wl.expert_outputs(w, N)
     want_out = oracle.combine(y, o["layout"]["token_pos"])
     dev = "cuda"
-    r = ep.route_nosync(idx.to(dev), wts.to(dev), w.P, w.E_local)
+    r = ep.route_nosync(idx.to(dev), wts.to(dev), w.P, w.E_local, with_tokens_per_expert=with_tpe)
     W = r["num_worst_rows"]
     recv = ep.dispatch_rows(x.to(dev), r["token_pos"], W, err=r["err"])
     y_pad = torch.zeros((W, w.H), dtype=torch.bfloat16, device=dev)
@@ -337,7 +339,8 @@ def test_route_nosync_matches_oracle(name):
     assert_equal("is_in_rank", np_(r["is_in_rank"]), oc["is_in_rank"])
     assert_equal("send_counts", np_(r["send_counts"]), oc["send_counts"])
     assert_equal("rank_offsets", np_(r["rank_offsets"]), np.concatenate([[0], np.cumsum(oc["send_counts"])]))
-    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), oc["tokens_per_expert"])
+    if with_tpe:
+        assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), oc["tokens_per_expert"])
     for k in ("send_token_idx", "send_rank", "send_idx"):
         assert_equal(k, np_(r[k])[:N], ol[k])
     assert_equal("send_w(bits)", np_(r["send_w"])[:N].view(np.uint32), ol["send_w"].view(np.uint32))
@@ -379,25 +382,62 @@ def test_route_nosync_capacity_is_flagged_and_bounded():
     assert_equal("rows below capacity", np_(sti[:cap]), ol["send_token_idx"][:cap])
 
 
+@pytest.mark.parametrize("with_tpe", [True, False])
 @pytest.mark.parametrize("T,H,K,P,E_local,fu,dup", EDGE)
-def test_route_nosync_edges(T, H, K, P, E_local, fu, dup):
+def test_route_nosync_edges(T, H, K, P, E_local, fu, dup, with_tpe):
     idx, wts = _routing(T, K, P * E_local, seed=T + H + 1, frac_unrouted=fu, dup=dup)
     o = oracle.send_path(_randn(T, 8, 2), idx, wts, None, P, E_local)
     N = o["layout"]["n"]
     dev = "cuda"
-    r = ep.route_nosync(idx.to(dev), wts.to(dev), P, E_local)
+    r = ep.route_nosync(idx.to(dev), wts.to(dev), P, E_local, with_tokens_per_expert=with_tpe)
     torch.cuda.synchronize()
     assert int(r["err"].item()) == 0
     oc, ol = o["counts"], o["layout"]
     assert_equal("dest", np_(r["dest"]), oc["dest"])
     assert_equal("is_in_rank", np_(r["is_in_rank"]), oc["is_in_rank"])
     assert_equal("send_counts", np_(r["send_counts"]), oc["send_counts"])
-    assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), oc["tokens_per_expert"])
+    if with_tpe:
+        assert_equal("tokens_per_expert", np_(r["tokens_per_expert"]), oc["tokens_per_expert"])
     assert int(r["rank_offsets"][P].item()) == N
     for k in ("send_token_idx", "send_rank", "send_idx"):
         assert_equal(k, np_(r[k])[:N], ol[k])
     assert_equal("send_w(bits)", np_(r["send_w"])[:N].view(np.uint32), ol["send_w"].view(np.uint32))
     assert_equal("token_pos", np_(r["token_pos"]), ol["token_pos"])
+
+
+@pytest.mark.parametrize("T,K,P,El", [(16385, 8, 8, 4), (32768, 6, 16, 4), (32769, 8, 8, 4), (30000, 3, 40, 2)])
+def test_route_nosync_larger_problems(T, K, P, El):
+    # the no-sync route without expert counts on larger problems (more than
+    # 32 ranks with a generic K among them), and ep_dispatch_nosync on the same
+    # inputs: both give the oracle's layout
+    idx, wts = _routing(T, K, P * El, seed=T + 5, frac_unrouted=0.1)
+    x = _randn(T, 16, 3)
+    o = oracle.send_path(x, idx, wts, None, P, El)
+    oc, ol = o["counts"], o["layout"]
+    N = ol["n"]
+    dev = "cuda"
+    r = ep.route_nosync(idx.to(dev), wts.to(dev), P, El, with_tokens_per_expert=False)
+    W = r["num_worst_rows"]
+    outs = {k: torch.full_like(r[k], -9) for k in ("dest", "is_in_rank", "send_counts", "rank_offsets",
+                                                    "send_token_idx", "send_rank", "send_idx", "send_w", "token_pos")}
+    recv = torch.empty((W, 16), dtype=torch.bfloat16, device=dev)
+    err = ep.error_word()
+    ep.ep_dispatch_nosync(x.to(dev), idx.to(dev), wts.to(dev), T, K, 16, P, El, W, 0, outs["dest"],
+                          outs["is_in_rank"], outs["send_counts"], outs["rank_offsets"], None, outs["send_token_idx"],
+                          outs["send_rank"], outs["send_idx"], outs["send_w"], outs["token_pos"], recv, None,
+                          ep.workspace(T, K, P, El), err)
+    torch.cuda.synchronize()
+    assert int(r["err"].item()) == 0 and int(err.item()) == 0
+    for g in (r, outs):
+        assert_equal("dest", np_(g["dest"]), oc["dest"])
+        assert_equal("is_in_rank", np_(g["is_in_rank"]), oc["is_in_rank"])
+        assert_equal("send_counts", np_(g["send_counts"]), oc["send_counts"])
+        assert int(g["rank_offsets"][P].item()) == N
+        for k in ("send_token_idx", "send_rank", "send_idx"):
+            assert_equal(k, np_(g[k])[:N], ol[k])
+        assert_equal("send_w(bits)", np_(g["send_w"])[:N].view(np.uint32), ol["send_w"].view(np.uint32))
+        assert_equal("token_pos", np_(g["token_pos"]), ol["token_pos"])
+    assert_equal("recv_x", bits16(recv)[:N], o["recv_x"])
 
 
 def test_route_nosync_repeated_calls_reuse_workspace():
