@@ -243,7 +243,8 @@ int ep_combine(const void *y, int64_t T, int H, const int32_t *token_pos, int P,
  *   x [T,H] bf16, topk_idx [T,K] int64, E = total experts (E % E_local == 0),
  *   tokens_per_expert [E_local] int32.
  *   ws: ep_workspace_size(T, K, E / E_local, E_local, 1) bytes, 256-byte
- *     aligned (the slots then take one cooperative launch when E_local <= 64).
+ *     aligned.  With E_local <= 64 the slots take one launch (one
+ *     thread-block cluster up to 32768 tokens, else a cooperative launch).
  * Device errors: EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_TIMEOUT. */
 int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K, int H,
                        int E, int E_local, int rank, int max_num_tokens,
