@@ -475,6 +475,7 @@ def run_gpu(args):
         result["other_paths"] = run_other_paths(ep, torch, wl, dev, flush, peak, iters=10)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, x_h, idx_h, w_h, y_h, args.cpu_steps, full=True)
+        result["cpu_baseline_threads"] = cpu_baseline_threads(w, x_h, idx_h, w_h, y_h, args.cpu_steps)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -744,6 +745,45 @@ def cpu_baseline(w, x, idx, wts, y, steps, full=True, T_sample=None):
     return {"value": round(T * steps / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{steps} step(s) of the send path (counts, layout, dispatch, combine) on the first "
                       f"{T} of {w.T} tokens of the {w.name} workload, single-threaded C oracle"}
+
+
+def oracle_step_threads(oracle, w, x, idx, wts, y, pool, parts):
+    """The same send path with the oracle's own functions, its independent
+    parts split over threads (ctypes releases the GIL): counts and layout
+    once, then the row gather on contiguous row ranges and the combine on
+    contiguous token ranges (each row and each token depends on nothing
+    else), so the result is the single-threaded one, bit for bit."""
+    import numpy as np
+    c = oracle.compute_send_counts(idx, w.P, w.E_local)
+    lay = oracle.build_send_layout(idx, wts, c["dest"], c["is_in_rank"], w.E_local)
+    sti, tp = lay["send_token_idx"], lay["token_pos"]
+    N, T = sti.size, tp.shape[0]
+    rb = [N * i // parts for i in range(parts + 1)]
+    tb = [T * i // parts for i in range(parts + 1)]
+    recv = list(pool.map(lambda i: oracle.dispatch(x, sti[rb[i]:rb[i + 1]]), range(parts)))
+    out = list(pool.map(lambda i: oracle.combine(y[:N], tp[tb[i]:tb[i + 1]]), range(parts)))
+    return recv, np.concatenate(out)
+
+
+def cpu_baseline_threads(w, x, idx, wts, y, steps):
+    """The oracle's send path over the host's cores (see oracle_step_threads);
+    checked bit for bit against the single-threaded oracle first."""
+    import concurrent.futures as cf
+    import numpy as np
+    import oracle
+    cores = max(1, min(os.cpu_count() or 1, 64))
+    with cf.ThreadPoolExecutor(cores) as pool:
+        _, out = oracle_step_threads(oracle, w, x, idx, wts, y, pool, cores)
+        if not np.array_equal(out, oracle_step(oracle, w, x, idx, wts, y)):
+            return {"unavailable": "the threaded oracle differs from the single-threaded one"}
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            oracle_step_threads(oracle, w, x, idx, wts, y, pool, cores)
+        dt = time.perf_counter() - t0
+    return {"value": round(w.T * steps / dt, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} step(s) of the send path on all {w.T} tokens of the {w.name} workload: the "
+                      f"single-threaded C oracle's counts and layout, then its row gather and combine on "
+                      f"{cores} row and token ranges in {cores} threads (same bits as one thread)"}
 
 
 def run_reference(args):
