@@ -91,6 +91,9 @@ __device__ __forceinline__ int group_owner_u(int lane)
 //   power of two:       scale = 2^e, the smallest power of two >= a / 448 (from
 //                       the bits of the fp32 quotient), q = e4m3_rn_satfinite(x * 2^-e),
 //                       UE8M0 code e + 127.
+// NaN elements do not enter the maximum (fmaxf).  A group holding +-inf has
+// a = inf: scale +inf and reciprocal +0 in both forms (UE8M0 code 255), so
+// its finite elements give +-0 and its infinities NaN codes.
 template <int U, bool RS>
 __device__ __forceinline__ void quantize_chunk(const uint4 (&vin)[U], int lane, uint2 (&q)[U], float &scale_own,
                                                uint32_t &code_own)
@@ -112,7 +115,7 @@ __device__ __forceinline__ void quantize_chunk(const uint4 (&vin)[U], int lane, 
         const uint32_t b = __float_as_uint(__fdiv_rn(a, 448.0f));
         const uint32_t eb = (b >> 23) + ((b & 0x7fffffu) != 0u);
         scale_own = __uint_as_float(eb << 23);
-        inv_own = __uint_as_float((254u - eb) << 23);
+        inv_own = eb < 255u ? __uint_as_float((254u - eb) << 23) : 0.0f;   // a = inf: 1 / inf
         code_own = eb;
     } else {
         inv_own = __fdiv_rn(448.0f, a);

@@ -46,6 +46,12 @@
  *     so x / scale never exceeds 448; the UE8M0 code is its biased exponent;
  *     four codes pack into an int32 with group 4j+i at byte i (least
  *     significant first);
+ *   - non-finite inputs to the fp8 quantisers: NaN elements do not enter the
+ *     group maximum; a group holding +-inf has a = inf, so scale = +inf and
+ *     the reciprocal is +0 in both forms (the plain form by IEEE division;
+ *     the power-of-two form by the same choice, UE8M0 code 255): its finite
+ *     elements give +-0 codes and its infinities and NaNs NaN codes, whose
+ *     sign IEEE leaves to the implementation;
  *   - capacity: an expert keeps its first `capacity` tokens in token order,
  *     later ones are dropped and counted (no error bit); capacity from a
  *     factor is ceil(factor * T * K / E);
@@ -473,6 +479,7 @@ void orc_batched_combine(const uint16_t *y, const int64_t *topk_idx, const float
 /*   q_i    = e4m3_rn_satfinite(x_i * (1 / scale))   (1/scale is exact)      */
 /*   code   = e + 127 where scale = 2^e (UE8M0: 8 exponent bits, bias 127,   */
 /*            no sign, no mantissa)                                          */
+/* A group holding +-inf: scale +inf, 1/scale = +0, code 255.                */
 /* ------------------------------------------------------------------------ */
 void orc_quantize_fp8_rows_pow2(const uint16_t *x, int64_t rows, int H, uint8_t *q, float *scale,
                                 uint8_t *code)
@@ -490,11 +497,18 @@ void orc_quantize_fp8_rows_pow2(const uint16_t *x, int64_t rows, int H, uint8_t 
             float a = amax > 1e-4f ? amax : 1e-4f;
             float s0 = a / 448.0f;
             int e;
-            float m = frexpf(s0, &e);        /* s0 = m * 2^e, 0.5 <= m < 1 */
-            if (m == 0.5f)
-                e -= 1;                      /* s0 is itself a power of two */
-            float sc = ldexpf(1.0f, e);
-            float inv = ldexpf(1.0f, -e);
+            float sc, inv;
+            if (isinf(s0)) {                 /* a group holding +-inf: no power of two covers it; */
+                e = 128;                     /* scale +inf, reciprocal +0 as 448/a gives the plain */
+                sc = INFINITY;               /* form, code 255 (the exponent field of +inf)        */
+                inv = 0.0f;
+            } else {
+                float m = frexpf(s0, &e);    /* s0 = m * 2^e, 0.5 <= m < 1 */
+                if (m == 0.5f)
+                    e -= 1;                  /* s0 is itself a power of two */
+                sc = ldexpf(1.0f, e);
+                inv = ldexpf(1.0f, -e);
+            }
             for (int i = 0; i < 128; ++i)
                 q[r * H + (int64_t)g * 128 + i] = orc_f32_to_e4m3(orc_bf16_to_f32(xs[i]) * inv);
             scale[r * G + g] = sc;

@@ -166,3 +166,60 @@ def test_capacity_drop():
     assert r["err"] & oracle.ERR_CAPACITY
     assert np.all(r["tokens_per_expert"] == M)
     assert r["slot"].max() == M - 1
+
+
+# Non-finite inputs (the pages are silent; the reading: NaN elements do not
+# enter a group's maximum, and a group holding +-inf has a = inf, so its scale
+# is +inf and its reciprocal +0 in both forms).  Pinned by IEEE arithmetic:
+# x * (+0) is +-0 with x's sign for finite x and NaN for +-inf or NaN.
+NAN16, INF16, NINF16 = 0x7FC0, 0x7F80, 0xFF80
+
+
+def _nonfinite_row():
+    f = np.zeros((1, 512), np.float32)
+    f[0, 128:131] = [3.0, -1.5, 0.25]          # group 1: finite, with a NaN at column 131
+    f[0, 256:259] = [1.0, -2.0, 7.0]           # group 2: finite, with +inf at 259 and -inf at 260
+    f[0, 384:387] = [5.0, -6.0, 0.5]           # group 3: finite only
+    x = _bf16(f)
+    x[0, 0] = NAN16                            # group 0: NaN and zeros only
+    x[0, 131] = NAN16
+    x[0, 259] = INF16
+    x[0, 260] = NINF16
+    return x
+
+
+def _is_nan_code(c):
+    return (np.asarray(c) & 0x7F) == 0x7F
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quantisers_on_non_finite_inputs(pow2):
+    x = _nonfinite_row()
+    if pow2:
+        q, s, c = oracle.quantize_fp8_rows_pow2(x)
+    else:
+        q, s = oracle.quantize_fp8_rows(x)
+    # NaN elements do not enter the maximum: groups 0, 1 and 3 are quantised
+    # exactly as with their NaNs replaced by +0, except the NaN's own code
+    clean = x.copy()
+    clean[0, 0] = 0
+    clean[0, 131] = 0
+    clean[0, 259:261] = 0
+    qc = oracle.quantize_fp8_rows_pow2(clean) if pow2 else oracle.quantize_fp8_rows(clean)
+    for g in (0, 1, 3):
+        cols = np.arange(g * 128, (g + 1) * 128)
+        keep = (cols != 0) & (cols != 131)
+        assert np.array_equal(q[0, cols[keep]], qc[0][0, cols[keep]]), g
+        assert s[0, g] == qc[1][0, g], g
+        if pow2:
+            assert c[0, g] == qc[2][0, g], g
+    assert _is_nan_code(q[0, 0]) and _is_nan_code(q[0, 131])
+    # group 0 holds only a NaN and zeros: the floor a = 1e-4 applies
+    assert s[0, 0] == qc[1][0, 0]
+    # group 2 holds +-inf: scale +inf, finite elements -> +-0, infinities -> NaN codes
+    assert s[0, 2] == np.inf
+    assert q[0, 256] == 0x00 and q[0, 257] == 0x80 and q[0, 258] == 0x00
+    assert np.all(q[0, 261:384] == 0x00)
+    assert _is_nan_code(q[0, 259]) and _is_nan_code(q[0, 260])
+    if pow2:
+        assert c[0, 2] == 255
