@@ -191,7 +191,9 @@ int ep_route_nosync_aligned(const int64_t *topk_idx, const float *topk_weights, 
  *     fp32, quantised per token in 1x128 groups: a = max(max|x|, 1e-4),
  *     q = e4m3_rn_satfinite(x * (448/a)), scale = a/448 (fp32, round to
  *     nearest even); every row sent for a token carries the same bytes.
- *     Needs H % 128 == 0.
+ *     NaN elements do not enter the maximum; a group holding +-inf has
+ *     scale +inf and reciprocal +0 (finite elements give +-0 codes,
+ *     infinities and NaNs NaN codes).  Needs H % 128 == 0.
  * Device errors: EP_ERR_COUNT_MISMATCH (a token_pos entry >= num_send). */
 int ep_dispatch(const void *x, int64_t T, int H, const int32_t *token_pos, int P,
                 int64_t num_send, void *recv_x, float *recv_scale, int fp8,
@@ -273,6 +275,8 @@ int ep_batched_prepare(const void *x, const int64_t *topk_idx, int64_t T, int K,
  *   round_scale = 1: scale = the smallest power of two >= a/448 (the fp32
  *     quotient), q = e4m3_rn_satfinite(x / scale) (exact division); its UE8M0
  *     code is log2(scale) + 127.
+ *   Non-finite inputs, both forms: NaN elements do not enter the maximum; a
+ *   group holding +-inf has scale +inf, reciprocal +0 and UE8M0 code 255.
  * zero_pad != 0 zero-fills the codes and scale entries of slots at or past
  * tokens_per_expert (the page's zero-initialised outputs); otherwise they are
  * left untouched.  b_q 16-byte aligned, b_scale 4-byte aligned; ws as for
