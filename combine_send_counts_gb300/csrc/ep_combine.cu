@@ -407,13 +407,14 @@ static int launch_gather_tma(const void *y, int64_t T, int H, const Rows &rows, 
     GatherGeom g = gather_geometry(H, D);
     const size_t smem = gather_smem_bytes(g);
     auto kernel = gather_tma_kernel<Rows, WEIGHTED, OUT_F32>;
-    static std::atomic<size_t> smem_set{0};   // per instantiation; raising the limit is idempotent
-    if (smem > smem_set.load(std::memory_order_relaxed)) {
+    static PerDevice smem_set;   // per instantiation and device; raising the limit is idempotent
+    const int dev = current_device();
+    if ((int)smem > smem_set.get(dev)) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
             cudaGetLastError();
             return EP_ERR_CUDA;
         }
-        smem_set.store(smem, std::memory_order_relaxed);
+        smem_set.put(dev, (int)smem);
     }
     const int64_t items = T * g.nchunk;
     if (items >= ((int64_t)1 << 30))

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the translation units of libep_gb300.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -22,8 +23,34 @@ inline int launch_status()
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
-// Attributes of the current device, read on first use and kept (the library
-// runs on one kind of GPU; concurrent first calls may both read them).
+// The current device (cudaGetDevice), or -1 if there is none.
+int current_device();
+
+// A non-negative value kept per device after its first lookup.  Function
+// attributes belong to the context of the device that was current when they
+// were set, and device attributes and occupancies may differ between
+// devices, so the launch policies keep theirs per device.  Zero-initialised
+// storage reads as "not yet known" (the value is stored plus one); devices
+// past kMaxDevices are not cached.  Concurrent first calls may both look the
+// value up and store the same result.
+constexpr int kMaxDevices = 64;
+class PerDevice {
+public:
+    int get(int dev) const   // -1 if not yet known
+    {
+        return dev >= 0 && dev < kMaxDevices ? v_[dev].load(std::memory_order_relaxed) - 1 : -1;
+    }
+    void put(int dev, int v)
+    {
+        if (dev >= 0 && dev < kMaxDevices)
+            v_[dev].store(v + 1, std::memory_order_relaxed);
+    }
+
+private:
+    std::atomic<int> v_[kMaxDevices];
+};
+
+// Attributes of the current device, read on its first use and kept.
 int device_sm_count();        // streaming multiprocessors (152 if unreadable)
 int64_t device_l2_bytes();    // L2 cache size in bytes (0 if unreadable)
 

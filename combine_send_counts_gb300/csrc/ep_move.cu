@@ -485,10 +485,20 @@ static cudaError_t launch_kernel(bool dependent, void (*kernel)(KArgs...), dim3 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-static int device_attribute(cudaDeviceAttr attr, int fallback)
+int current_device()
 {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev;
+}
+
+static int device_attribute(int dev, cudaDeviceAttr attr, int fallback)
+{
+    int v = 0;
+    if (dev < 0 || cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v < 0) {
         cudaGetLastError();
         return fallback;
     }
@@ -497,22 +507,24 @@ static int device_attribute(cudaDeviceAttr attr, int fallback)
 
 int device_sm_count()
 {
-    static std::atomic<int> sms{0};
-    int v = sms.load(std::memory_order_relaxed);
-    if (v == 0) {
-        v = device_attribute(cudaDevAttrMultiProcessorCount, 152);
-        sms.store(v, std::memory_order_relaxed);
+    static PerDevice sms;
+    const int dev = current_device();
+    int v = sms.get(dev);
+    if (v < 0) {
+        v = device_attribute(dev, cudaDevAttrMultiProcessorCount, 152);
+        sms.put(dev, v);
     }
     return v;
 }
 
 int64_t device_l2_bytes()
 {
-    static std::atomic<int> bytes{-1};
-    int v = bytes.load(std::memory_order_relaxed);
+    static PerDevice bytes;
+    const int dev = current_device();
+    int v = bytes.get(dev);
     if (v < 0) {
-        v = device_attribute(cudaDevAttrL2CacheSize, 0);
-        bytes.store(v, std::memory_order_relaxed);
+        v = device_attribute(dev, cudaDevAttrL2CacheSize, 0);
+        bytes.put(dev, v);
     }
     return v;
 }
@@ -591,8 +603,9 @@ static int launch_scatter_fp8_units(const void *x, int64_t T, int H, const Batch
     const int nvec = H / 8;
     const bool u4 = nvec > 64;
     auto kernel = u4 ? scatter_fp8_units_kernel<4, SF, RS> : scatter_fp8_units_kernel<2, SF, RS>;
-    static std::atomic<int> per_sm_cache[2] = {{-1}, {-1}};
-    int per_sm = per_sm_cache[u4].load(std::memory_order_relaxed);
+    static PerDevice per_sm_cache[2];
+    const int dev = current_device();
+    int per_sm = per_sm_cache[u4].get(dev);
     if (per_sm < 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kMoveThreads, 0) != cudaSuccess) {
@@ -600,7 +613,7 @@ static int launch_scatter_fp8_units(const void *x, int64_t T, int H, const Batch
             n = 0;
         }
         per_sm = std::max(n, 1);
-        per_sm_cache[u4].store(per_sm, std::memory_order_relaxed);
+        per_sm_cache[u4].put(dev, per_sm);
     }
     const int chunk = 32 * (u4 ? 4 : 2);
     const int64_t units = T * ((nvec + chunk - 1) / chunk);

@@ -134,9 +134,10 @@ extern "C" int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk
     // the next token's slots loaded ahead: on 32 K tokens this beat one warp
     // per token (16.3 -> 14.3 us; the same at 16 K tokens), since short-lived
     // blocks pay their scheduling in every wave
-    static std::atomic<int> resident[2] = {{0}, {0}};   // blocks per SM, [vec]
-    int per_sm = resident[vec ? 1 : 0].load(std::memory_order_relaxed);
-    if (per_sm == 0) {
+    static PerDevice resident[2];   // blocks per SM, [vec]
+    const int dev = current_device();
+    int per_sm = resident[vec ? 1 : 0].get(dev);
+    if (per_sm < 0) {
         int n = 0;
         const cudaError_t e = vec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, multihot_kernel<true>,
                                                                                  kMultihotThreads, 0)
@@ -147,7 +148,7 @@ extern "C" int ep_indices_to_multihot(const int64_t *topk_idx, const float *topk
             n = 4;
         }
         per_sm = std::max(n, 1);
-        resident[vec ? 1 : 0].store(per_sm, std::memory_order_relaxed);
+        resident[vec ? 1 : 0].put(dev, per_sm);
     }
     const int64_t blocks = std::min<int64_t>(ceil_div(T, kMultihotWarps), (int64_t)per_sm * device_sm_count());
     if (vec)

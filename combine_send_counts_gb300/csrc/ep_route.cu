@@ -948,9 +948,10 @@ static int launch_route_fused(const FusedArgs &a, int nb, size_t smem, cudaStrea
     *launched = false;
     // blocks per SM, [counting experts?]; with dynamic shared memory the
     // count depends on smem, which a call with expert counts passes as E ints
-    static std::atomic<int> max_per_sm[2] = {{-1}, {-1}};
+    static PerDevice max_per_sm[2];
     const int slot = smem > 0 ? 1 : 0;
-    int per_sm = max_per_sm[slot].load(std::memory_order_relaxed);
+    const int dev = current_device();
+    int per_sm = max_per_sm[slot].get(dev);
     if (per_sm < 0 || slot == 1) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_fused_kernel<KC>, kFusedThreads, smem) != cudaSuccess) {
@@ -958,7 +959,7 @@ static int launch_route_fused(const FusedArgs &a, int nb, size_t smem, cudaStrea
             n = 0;
         }
         per_sm = n;
-        max_per_sm[slot].store(n, std::memory_order_relaxed);
+        max_per_sm[slot].put(dev, n);
     }
     if ((int64_t)per_sm * device_sm_count() < nb)
         return EP_OK;   // cannot be co-resident: the caller falls back to two launches
@@ -1127,8 +1128,9 @@ template <int KC>
 static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t stream, bool *launched)
 {
     *launched = false;
-    static std::atomic<int> max_per_sm{-1};
-    int per_sm = max_per_sm.load(std::memory_order_relaxed);
+    static PerDevice max_per_sm;
+    const int dev = current_device();
+    int per_sm = max_per_sm.get(dev);
     if (per_sm < 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, batched_fused_kernel<KC>, kFusedThreads, 0) != cudaSuccess) {
@@ -1136,7 +1138,7 @@ static int launch_batched_fused(const BatchedFusedArgs &a, int nb, cudaStream_t 
             n = 0;
         }
         per_sm = n;
-        max_per_sm.store(n, std::memory_order_relaxed);
+        max_per_sm.put(dev, n);
     }
     const int sms = device_sm_count();
     if ((int64_t)per_sm * sms < nb)
@@ -1351,8 +1353,9 @@ __global__ void __launch_bounds__(kClThreads, 1) batched_cluster_kernel(BatchedC
 template <int KC>
 static int batched_cluster_size()
 {
-    static std::atomic<int> size{-1};
-    int n = size.load(std::memory_order_relaxed);
+    static PerDevice size;   // the attributes below are set per device
+    const int dev = current_device();
+    int n = size.get(dev);
     if (n >= 0)
         return n;
     n = 0;
@@ -1381,7 +1384,7 @@ static int batched_cluster_size()
         }
         cudaGetLastError();
     }
-    size.store(n, std::memory_order_relaxed);
+    size.put(dev, n);
     return n;
 }
 
