@@ -508,8 +508,9 @@ def combine(local_out: torch.Tensor, handle: dict, dtype=None):
 
 
 def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int,
-                    zero_pad: bool = False, err=None, stream=None):
-    """-> dict(b_x [E_local,M,H], tokens_per_expert [E_local], slot [T,K])."""
+                    zero_pad: bool = False, err=None, stream=None, ws=None):
+    """-> dict(b_x [E_local,M,H], tokens_per_expert [E_local], slot [T,K]).
+    ws: a workspace of at least ep_workspace_size bytes, or None for a new one."""
     _expect("batched_prepare", x=(x, torch.bfloat16), topk_idx=(topk_idx, torch.int64))
     T, H = x.shape
     K = topk_idx.shape[1]
@@ -518,7 +519,7 @@ def batched_prepare(x, topk_idx, num_experts: int, num_local_experts: int, rank:
     b_x = torch.empty((El, max_num_tokens, H), dtype=x.dtype, device=dev)
     tpe = torch.empty(El, dtype=torch.int32, device=dev)
     slot = torch.empty((T, K), dtype=torch.int32, device=dev)
-    ws = workspace(T, K, num_experts // El, El, 1, dev)
+    ws = ws if ws is not None else workspace(T, K, num_experts // El, El, 1, dev)
     err = err if err is not None else error_word(dev)
     ep_batched_prepare(x, topk_idx, T, K, H, num_experts, El, rank, max_num_tokens, b_x, tpe, slot,
                        int(zero_pad), ws, err, stream)
@@ -579,10 +580,11 @@ def expert_capacity(num_tokens: int, topk: int, num_experts: int, capacity_facto
 
 def batched_prepare_ex(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int, *,
                        capacity: int = 0, alignment: int = 1, scale_fmt: Optional[int] = None,
-                       round_scale: bool = False, zero_pad: bool = False, err=None, stream=None):
+                       round_scale: bool = False, zero_pad: bool = False, err=None, stream=None, ws=None):
     """Expert-batched prepare with a per-expert capacity (0: max_num_tokens,
     overflow is an error; else later tokens are dropped and counted) and a
     receive alignment.  scale_fmt None: bf16 rows; else fp8 codes + scales.
+    ws: a workspace of at least ep_workspace_size bytes, or None for a new one.
     -> dict(b_rows, b_scale, tokens_per_expert, slot, dropped, err)."""
     _expect("batched_prepare_ex", x=(x, torch.bfloat16), topk_idx=(topk_idx, torch.int64))
     T, H = x.shape
@@ -598,7 +600,7 @@ def batched_prepare_ex(x, topk_idx, num_experts: int, num_local_experts: int, ra
     tpe = torch.empty(El, dtype=torch.int32, device=dev)
     slot = torch.empty((T, K), dtype=torch.int32, device=dev)
     dropped = torch.empty(El, dtype=torch.int32, device=dev)
-    ws = workspace(T, K, num_experts // El, El, 1, dev)
+    ws = ws if ws is not None else workspace(T, K, num_experts // El, El, 1, dev)
     err = err if err is not None else error_word(dev)
     ep_batched_prepare_ex(x, topk_idx, T, K, H, num_experts, El, rank, M, capacity, alignment, b_rows, b_s,
                           -1 if not fp8 else scale_fmt, int(round_scale), tpe, slot, dropped, int(zero_pad), ws,
@@ -619,9 +621,10 @@ def batched_scale_storage(E_local: int, M: int, H: int, scale_fmt: int):
 
 def batched_prepare_fp8(x, topk_idx, num_experts: int, num_local_experts: int, rank: int, max_num_tokens: int,
                         scale_fmt: int = EP_SCALE_ROW_F32, round_scale: bool = False, zero_pad: bool = False,
-                        err=None, stream=None):
+                        err=None, stream=None, ws=None):
     """-> dict(b_q [E_local,M,H] uint8 (e4m3 codes), b_scale (batched_scale_storage),
-    tokens_per_expert [E_local], slot [T,K])."""
+    tokens_per_expert [E_local], slot [T,K]).  ws: a workspace of at least
+    ep_workspace_size bytes, or None for a new one."""
     _expect("batched_prepare_fp8", x=(x, torch.bfloat16), topk_idx=(topk_idx, torch.int64))
     T, H = x.shape
     K = topk_idx.shape[1]
@@ -632,7 +635,7 @@ def batched_prepare_fp8(x, topk_idx, num_experts: int, num_local_experts: int, r
     b_s = torch.empty(shape, dtype=dt, device=dev)
     tpe = torch.empty(El, dtype=torch.int32, device=dev)
     slot = torch.empty((T, K), dtype=torch.int32, device=dev)
-    ws = workspace(T, K, num_experts // El, El, 1, dev)
+    ws = ws if ws is not None else workspace(T, K, num_experts // El, El, 1, dev)
     err = err if err is not None else error_word(dev)
     ep_batched_prepare_fp8(x, topk_idx, T, K, H, num_experts, El, rank, max_num_tokens, b_q, b_s, scale_fmt,
                            int(round_scale), tpe, slot, int(zero_pad), ws, err, stream)

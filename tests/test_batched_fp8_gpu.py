@@ -164,3 +164,26 @@ def test_batched_fp8_every_slot_kernel_matches_oracle(T, H, K, E, El, rank, M, w
     assert int(err.item()) == 0, ep.ep_status_str(int(err.item()))
     o = oracle.batched_prepare_fp8(x, idx, E, El, rank, M, fmt, False)
     _compare(dict(tokens_per_expert=tpe, slot=slot, b_q=b_q, b_scale=b_s), o, fmt, check_all=False)
+
+
+def test_batched_helpers_take_a_callers_workspace():
+    # one workspace, reused by the three expert-batched helpers in turn
+    T, H, K, E, El, rank, M = 900, 512, 4, 32, 8, 2, 400
+    idx, _ = routing_inputs(T, K, E, 61, 0.1)
+    x = _wide_rows(T, H, 62)
+    ws = ep.workspace(T, K, E // El, El)
+    xd, idd = x.cuda(), idx.cuda()
+    r0 = ep.batched_prepare(xd, idd, E, El, rank, M, zero_pad=True, ws=ws)
+    r1 = ep.batched_prepare_fp8(xd, idd, E, El, rank, M, ep.EP_SCALE_COL_F32, False, zero_pad=True, ws=ws)
+    r2 = ep.batched_prepare_ex(xd, idd, E, El, rank, M, capacity=20, alignment=16, scale_fmt=ep.EP_SCALE_ROW_F32,
+                               zero_pad=True, ws=ws)
+    torch.cuda.synchronize()
+    o0 = oracle.batched_prepare(x, idx, E, El, rank, M, zero_pad=True)
+    assert_equal("bf16 rows", np_(r0["b_x"].view(torch.int16)).view(np.uint16), o0["b_x"])
+    assert_equal("bf16 slots", np_(r0["slot"]), o0["slot"])
+    _compare(r1, oracle.batched_prepare_fp8(x, idx, E, El, rank, M, ep.EP_SCALE_COL_F32, False, zero_pad=True),
+             ep.EP_SCALE_COL_F32, check_all=True)
+    o2 = oracle.batched_prepare_ex(x, idx, E, El, rank, M, 20, 16, fmt=oracle.SCALE_ROW_F32, zero_pad=True)
+    assert_equal("capacity rows", np_(r2["b_rows"]), o2["b_rows"])
+    assert_equal("capacity slots", np_(r2["slot"]), o2["slot"])
+    assert_equal("dropped", np_(r2["dropped"]), o2["dropped"])
