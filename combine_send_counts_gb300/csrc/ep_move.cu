@@ -12,8 +12,10 @@
 // The bf16 scatter is an HBM-bound copy.  A group of G threads (a multiple of
 // 32) owns one token; each thread moves U 16-byte vectors of the row, so a row
 // is covered in one pass for H up to 8*G*U.  The destination row list of the
-// block's tokens is resolved once into shared memory.  The fp8 scatter gives
-// each token one warp, which also computes the group scales.
+// block's tokens is resolved once into shared memory.  The fp8 scatter
+// quantises each row once, in warps that also compute the group scales: one
+// warp per token on the send layout, balanced runs of (token, 1024-column
+// chunk) units per warp on the expert-batched layout.
 #include <algorithm>
 #include <atomic>
 #include <type_traits>
