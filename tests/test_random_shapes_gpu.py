@@ -3,7 +3,9 @@ send layout, dispatch and combine (axolotl torch_dispatch; the host-sync and
 no-sync call orders, bf16 and fp8 payloads of NeMo uccl_ep.buffer
 Buffer.dispatch), the expert-batched prepare and weighted combine (vLLM
 BatchedPrepareAndFinalize, bf16 and every fp8 scale layout), and the multihot
-map (NeMo token_dispatcher _indices_to_multihot).
+map (NeMo token_dispatcher _indices_to_multihot), with capacity drops and
+receive alignment on both layouts (NeMo token_dispatcher capacity factor and
+pad multiple, uccl_ep.buffer expert_alignment).
 
 Each case draws P, E_local, K, T, H, the share of unrouted slots and
 whether ids repeat within a token, so that the kernels' template forms
@@ -139,6 +141,37 @@ def test_random_shape_matches_oracle(c):
         assert_equal("fp8 batched slot", np_(r8["slot"]), o8["slot"])
         assert_equal("fp8 batched codes", np_(r8["b_q"]), o8["b_q"])
         assert_equal("fp8 batched scales (bits)", np_(r8["b_scale"]).view(np.uint32), o8["b_scale"].view(np.uint32))
+
+    # capacity drops and receive alignment on the batched layout (bf16 or fp8 rows)
+    C = 1 + (c["seed"] * 7919) % M
+    A = [1, 4, 16, 128][c["seed"] % 4]
+    fx = ep.EP_SCALE_COL_F32 if c["fp8"] else None
+    ox = oracle.batched_prepare_ex(x, idx, E, El, rank, M, C, A, fmt=fx, zero_pad=True)
+    rx = ep.batched_prepare_ex(x.to(dev), idx.to(dev), E, El, rank, M, capacity=C, alignment=A, scale_fmt=fx,
+                               zero_pad=True)
+    torch.cuda.synchronize()
+    assert int(rx["err"].item()) == 0 and ox["err"] == 0
+    for k in ("slot", "tokens_per_expert", "dropped"):
+        assert_equal(k + " (capacity)", np_(rx[k]), ox[k])
+    rows = np_(rx["b_rows"]) if c["fp8"] else bits16(rx["b_rows"])
+    assert_equal("rows (capacity)", rows, ox["b_rows"])
+    if c["fp8"]:
+        assert_equal("scales (capacity, bits)", np_(rx["b_scale"]).view(np.uint32), ox["b_scale"].view(np.uint32))
+
+    # send layout with every rank segment aligned
+    Ar = [2, 4, 16, 128][(c["seed"] // 4) % 4]
+    ra = ep.route_nosync(idx.to(dev), w.to(dev), P, El, alignment=Ar)
+    torch.cuda.synchronize()
+    al = oracle.align_send_layout(o["layout"], o["counts"]["send_counts"], Ar)
+    n = al["n"]
+    assert int(ra["err"].item()) == 0
+    assert_equal("rank_offsets (aligned)", np_(ra["rank_offsets"]), al["rank_offsets"])
+    assert_equal("tokens_per_expert (aligned)", np_(ra["tokens_per_expert"]),
+                 -(-o["counts"]["tokens_per_expert"] // Ar) * Ar)
+    for k in ("send_token_idx", "send_rank", "send_idx"):
+        assert_equal(k + " (aligned)", np_(ra[k])[:n], al[k])
+    assert_equal("send_w (aligned, bits)", np_(ra["send_w"])[:n].view(np.uint32), al["send_w"].view(np.uint32))
+    assert_equal("token_pos (aligned)", np_(ra["token_pos"]), al["token_pos"])
 
     # multihot map and dense probabilities
     if T * E <= CAP:
